@@ -1,0 +1,384 @@
+#!/usr/bin/env python3
+"""Benchmark: verify attention over an int8 paged KV cache on one GB300.
+
+One step = one pass of the whole hot path over the workload's batch:
+``splash_kv_append`` of every sequence's verify block (quantise + scatter),
+then ``splash_verify_attention`` (split planner, attention kernels, log-sum-exp
+combine). Default workload: 16 sequences x 32768 cached tokens, 24 query / 4
+KV heads, head_dim 256, T = 16, int8 KV with 1% outlier channels. The KV cache
+(1.09 GB) is larger than L2 (129 MB), so no flush is needed between steps.
+
+Prints one JSON line. ``--impl reference`` times the fp64 CPU oracle (the
+reference arm: a slow, plain program) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from speculative_verify_attention_kv_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "verify tokens/s and achieved HBM GB/s (% of GB300 peak), 16×32K int8 KV"
+UNIT = "verify tokens/s"
+DEFAULT_WORKLOAD = "batch16_32k"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=[s.name for s in wl.SPECS])
+    ap.add_argument("--path", type=int, default=0, help="0 auto, 1 CUDA-core, 2 tensor-core")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args(argv)
+
+
+# ---- multi-rank plumbing (weak scaling: every rank runs its own batch) ------
+def rank_info():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def rank_seed(spec: wl.WorkloadSpec, rank: int) -> int:
+    """Each rank draws an independent batch of the same shape."""
+    return spec.seed + 7919 * rank
+
+
+def reduce_max(value: float, world: int, device=None) -> float:
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---- peaks, clocks, profiles -------------------------------------------------
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling during the timed region."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.TemporaryFile(mode="w+")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.seek(0)
+        rows = [r.split(",") for r in self.file.read().strip().splitlines() if r.strip()]
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[0]))
+                mx = max(mx, float(r[1]))
+                for n, v in zip(names, r[4:8]):
+                    if v.strip().lower() == "active":
+                        reasons.add(n)
+            except (ValueError, IndexError):
+                continue
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def kernel_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, or None when the
+    kernel source changed after the counters were taken."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        ent = d[f"{kernel}@{workload}"]
+    except (OSError, KeyError, ValueError):
+        return None
+    src = os.path.join(ROOT, "speculative_verify_attention_kv_gb300", "csrc", ent["source"])
+    try:
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    except OSError:
+        return None
+    return ent["bytes_per_launch"] if h == ent["source_sha"] else None
+
+
+# ---- CPU baseline: the fp64 oracle on a bounded sample ----------------------
+def oracle_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def cpu_baseline(W: wl.Workload, budget_s: float, max_steps: int | None = None):
+    """Times the oracle's step (append of a sequence's block + its attention) on
+    sampled sequences of the workload until ``budget_s`` of oracle time."""
+    from oracle import splash_oracle as O
+    s = W.spec
+    G = s.group
+    seqs = list(range(W.num_seqs))
+    rng = np.random.default_rng(0)
+    rng.shuffle(seqs)
+    elapsed, tokens, done, used = 0.0, 0, 0, []
+    for b in seqs:
+        if W.block_lens[b] == 0:
+            continue
+        pool = O.PagedPool(W.num_pages, s.num_kv_heads, s.page_size, s.head_dim)
+        ks, vs = [], []
+        for h in range(s.num_kv_heads):
+            k, v = W.context_kv(b, h)
+            ks.append(k)
+            vs.append(v)
+        O.kv_append(pool, np.stack(ks, 1), np.stack(vs, 1), W.page_table[b:b + 1], np.array([0]),
+                    np.array([int(W.context_lens[b])]))
+        bk, bv = W.block_kv_seq(b)
+        q = wl.f32_from_bf16_bits(W.q_bits_seq(b)).astype(np.float64)
+        T, ctx = int(W.block_lens[b]), int(W.context_lens[b])
+        t0 = time.perf_counter()
+        O.kv_append(pool, bk, bv, W.page_table[b:b + 1], W.context_lens[b:b + 1],
+                    W.block_lens[b:b + 1])
+        for h in range(s.num_kv_heads):
+            k, v = O.gather_keys(pool, W.page_table[b], h, ctx + T)
+            O.attention_seq_head(q[:, h * G:(h + 1) * G], k, v, ctx, float(W.sm_scale))
+        elapsed += time.perf_counter() - t0
+        tokens += T
+        done += 1
+        used.append(b)
+        if elapsed >= budget_s or (max_steps and done >= max_steps):
+            break
+    return {"value": tokens / elapsed, "unit": UNIT, "cores": oracle_threads(), "kind": "oracle",
+            "sample": f"{done} of {W.num_seqs} sequences of {W.spec.name} (append of the block + "
+                      f"all KV heads' attention), {elapsed:.1f} s of fp64 numpy"}, elapsed, tokens
+
+
+def run_reference(args):
+    rank, world, _ = rank_info()
+    if rank != 0:
+        return 0
+    W = wl.make(args.workload)
+    per_step = max(1.0, args.cpu_seconds / max(args.steps, 1))
+    for _ in range(args.warmup):
+        cpu_baseline(W, per_step, max_steps=1)
+    tot_t, tot_tok = 0.0, 0
+    for _ in range(args.steps):
+        _, t, n = cpu_baseline(W, per_step, max_steps=1)
+        tot_t += t
+        tot_tok += n
+    value = tot_tok / tot_t
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot_t / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded; stands in for the pages' coding prompts)",
+            "config": {"workload": W.spec.name, "seqs": W.num_seqs,
+                       "sample": "one sequence per step"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle_threads(),
+                             "kind": "oracle", "sample": "one sequence per step"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+# ---- GPU arm -------------------------------------------------------------------
+def run_ours(args):
+    import torch
+    rank, world, local = rank_info()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    from speculative_verify_attention_kv_gb300 import splash_kv as sk
+    from speculative_verify_attention_kv_gb300.device_workload import DeviceWorkload
+
+    spec = wl.SPEC_BY_NAME[args.workload]
+    W = wl.Workload(spec, rank_seed(spec, rank))
+    dw = DeviceWorkload(W)
+    stream = torch.cuda.current_stream()
+    n_tok = W.num_q_tokens
+    algo_bytes = W.algorithmic_bytes()
+
+    ev_a0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev_a1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+
+    def step(i=None):
+        dw.append_block()
+        ev = (ev_a0[i], ev_a1[i]) if i is not None else None
+        sk.splash_verify_attention(dw.q, *dw.pool, dw.table, dw.ctx, dw.T, float(W.sm_scale),
+                                   dw.max_T, dw.out, dw.lse, dw.ws, device_status=dw.status,
+                                   path=args.path, events=ev)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    if int(dw.status.item()) != 0:
+        raise RuntimeError(f"device status {int(dw.status.item())}")
+
+    clocks = ClockSampler(torch.cuda.current_device())
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ck = clocks.stop()
+    barrier(world)
+    ms = t0.elapsed_time(t1) / args.steps
+    ms_max = reduce_max(ms, world)
+    attn_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(ev_a0, ev_a1))
+
+    # end to end through the public API with host buffers: H2D of the step's
+    # inputs (q, k_new, v_new, lengths) from pinned memory, append + attention,
+    # D2H of out + lse, every step.
+    h_q = dw.q.cpu().pin_memory()
+    h_k = dw.k_new.cpu().pin_memory()
+    h_v = dw.v_new.cpu().pin_memory()
+    h_ctx = dw.ctx.cpu().pin_memory()
+    h_T = dw.T.cpu().pin_memory()
+    h_out = torch.empty(dw.out.shape, dtype=dw.out.dtype).pin_memory()
+    h_lse = torch.empty(dw.lse.shape, dtype=dw.lse.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_ctx, h_T))
+    d2h = sum(t.numel() * t.element_size() for t in (h_out, h_lse))
+
+    def e2e_step():
+        dw.q.copy_(h_q, non_blocking=True)
+        dw.k_new.copy_(h_k, non_blocking=True)
+        dw.v_new.copy_(h_v, non_blocking=True)
+        dw.ctx.copy_(h_ctx, non_blocking=True)
+        dw.T.copy_(h_T, non_blocking=True)
+        dw.step()
+        h_out.copy_(dw.out, non_blocking=True)
+        h_lse.copy_(dw.lse, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = reduce_max(e0.elapsed_time(e1) / args.steps, world)
+
+    peak, peak_src = load_peaks()
+    achieved = algo_bytes / (attn_ms * 1e-3) / 1e9
+    attn_kernel = "verify_tc" if args.path == 2 else "verify_attention"
+    line = {
+        "metric": METRIC,
+        "value": world * n_tok / (ms_max * 1e-3),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": max(args.warmup, 3),
+        "ms_per_step": ms_max,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "int8 KV / bf16 Q,O / fp32 accumulate",
+        "data": "synthetic (seeded; stands in for the pages' coding prompts)",
+        "config": {"workload": W.spec.name, "seqs": W.num_seqs, "context": int(W.context_lens.max()),
+                   "verify_block": int(W.block_lens.max()), "q_heads": spec.num_q_heads,
+                   "kv_heads": spec.num_kv_heads, "head_dim": spec.head_dim, "page": spec.page_size,
+                   "verify_tokens_per_step": n_tok, "algorithmic_bytes": algo_bytes,
+                   "l2": "inputs larger than L2 (KV cache > 129 MB), no flush",
+                   "attention_ms": attn_ms, "hbm_gbs": achieved, "hbm_frac": achieved / peak,
+                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_source": f"{peak_src} (hbm_gbs, of {peak_src})",
+                     "kernel": attn_kernel,
+                     "traffic": kernel_traffic(attn_kernel, W.spec.name)},
+        "e2e": {"value": world * n_tok / (e2e_ms * 1e-3), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps * dw_launches_per_step(W, args.path),
+        "clocks": ck,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        cb, _, _ = cpu_baseline(W, args.cpu_seconds)
+        line["cpu_baseline"] = cb
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def dw_launches_per_step(W: wl.Workload, path: int) -> int:
+    """Kernels one step launches: append, planner, attention kernel(s), combine."""
+    from speculative_verify_attention_kv_gb300 import splash_kv as sk
+    tc = sk.tensor_path_available(W.spec.head_dim)
+    # automatic mode with the tensor-core kernel launches both kernels (one may find no work)
+    n_attn = 2 if (path == 0 and tc) else 1
+    return 1 + 1 + n_attn + 1
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,185 @@
+/*
+ * splash_kv.h — C ABI of the int8 paged-KV verify-attention library (GB300, sm_103a).
+ *
+ * The operation. In-batch speculative decoding as the Splash engine describes it
+ * ("Splash: 범용 엔진 대신 모델마다 커널과 초안 모델을 새로 만드는 Apple Silicon 추론
+ * 엔진", discuss.pytorch.kr; section "옵션이 아니라 기본 경로인 DFlash 2 추측
+ * 디코딩"): every sequence submits a block of T draft tokens that the target
+ * model verifies in one forward pass, each sequence with its own T. Attention
+ * state lives in a paged KV cache indexed by prefix, so sequences that share a
+ * prefix share its pages (section "배치 스케줄링과 시작 시점에 확정되는 메모리
+ * 예산"). The decode kernel reads the 8-bit KV cache directly and reuses each
+ * KV tile across the query heads of a GQA group and across the verify tokens
+ * (section "형상에 맞춰 자동으로 생성하는 Metal 커널"). The bnskd.com article
+ * ("Splash：把推理引擎「围着模型造」…", section "技术内核") states the same.
+ * The pages fix no quantisation scheme, layout, mask or precision; the ones
+ * below are this library's readings.
+ *
+ * Conventions for every entry point
+ *   - Pointers named *_pages, *_scales, q, out, lse, page_table, *_lens,
+ *     k_new, v_new, workspace and device_status are DEVICE pointers owned by
+ *     the caller. The library never allocates, frees or synchronises; all work
+ *     is enqueued on `stream` (NULL = legacy default stream) and is async.
+ *   - Return value: SPLASH_OK or a negative SPLASH_ERR_* code. Argument errors
+ *     are detected on the host BEFORE anything is launched. A CUDA launch error
+ *     returns SPLASH_ERR_CUDA (the CUDA error is left for cudaGetLastError).
+ *   - Errors only visible on the device (a page id out of range or -1 where a
+ *     page is needed, a length out of range) never trap: the kernel skips the
+ *     affected work and, when device_status is non-NULL, stores the first such
+ *     SPLASH_DEVICE_* code there (atomic compare-and-swap from 0). The caller
+ *     zeroes *device_status before the call and reads it after the stream syncs.
+ *
+ * Shapes and layouts (row-major, innermost last)
+ *   Hq = num_q_heads, Hkv = num_kv_heads, G = Hq / Hkv (query head hq uses KV
+ *   head hq / G), D = head_dim in {64, 128, 256}, P = page_size = 16.
+ *   k_pages, v_pages : int8  [num_pages, Hkv, P, D]   codes
+ *   k_scales, v_scales: fp32 [num_pages, Hkv, P]      one scale per (token, KV head)
+ *   page_table       : int32 [num_seqs, max_pages_per_seq]; logical position j of
+ *                      sequence b lives in page page_table[b][j / P], slot j % P.
+ *                      Entries past a sequence's needed pages are ignored (-1 is
+ *                      the customary sentinel). Pages may be shared between
+ *                      sequences (shared prefix); they are read-only to attention.
+ *   context_lens     : int32 [num_seqs] tokens cached before the block (ctx_b >= 0)
+ *   block_lens       : int32 [num_seqs] verify-block length T_b >= 0 (0 = idle)
+ *   Tokens of all blocks are packed by sequence: sequence b owns rows
+ *   sum(block_lens[0..b-1]) .. + T_b - 1 of q / k_new / v_new / out / lse.
+ */
+#ifndef SPLASH_KV_H
+#define SPLASH_KV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st; /* cudaStream_t */
+
+enum {
+  SPLASH_OK = 0,
+  SPLASH_ERR_INVALID_ARGUMENT = -1,   /* null pointer, negative size, Hq % Hkv != 0 ... */
+  SPLASH_ERR_UNSUPPORTED = -2,        /* D not in {64,128,256}, P != 16, T*G too large */
+  SPLASH_ERR_WORKSPACE_TOO_SMALL = -3,
+  SPLASH_ERR_CUDA = -4                /* a kernel launch failed */
+};
+
+enum {
+  SPLASH_DEVICE_BAD_PAGE = 1,         /* page id < 0 or >= num_pages where a page is needed */
+  SPLASH_DEVICE_BAD_LENGTH = 2        /* ctx or T negative, T > max_block_len, or
+                                         ctx + T > max_pages_per_seq * P */
+};
+
+/* Human-readable name of a SPLASH_* status (static string, never NULL). */
+const char* splash_status_string(int status);
+
+/* Library ABI version (increments on any signature change). */
+int splash_abi_version(void);
+
+/* 1 if the tensor-core attention kernel is built for this head_dim, else 0
+ * (units then run on the CUDA-core kernel). */
+int splash_tensor_path_supported(int head_dim);
+
+/*
+ * splash_kv_append — quantise a block of new K/V rows to int8 and write them
+ * into the pages.
+ *
+ * For every sequence b and t < T_b, row r = sum(block_lens[0..b-1]) + t of
+ * k_new / v_new (fp32 [num_new_tokens, Hkv, D]) is written at logical position
+ * context_lens[b] + t, separately per KV head:
+ *   a = max_d |x_d|;  s = fl32(a / 127);  c_d = clamp(rne(fl32(x_d / s)), -127, 127)
+ *   (s == 0 gives all-zero codes), with correctly rounded fp32 division and
+ *   round-half-to-even. Codes go to k_pages / v_pages, s to k_scales / v_scales.
+ * num_new_tokens must equal sum(block_lens) (not checked on the host, which
+ * cannot read device memory; rows past the sum are ignored). The target slots
+ * must not be shared with another sequence (copy-on-write is the caller's).
+ * Populating a cache uses the same call with context_lens = start positions.
+ */
+int splash_kv_append(const float* k_new, const float* v_new, int num_new_tokens,
+                     int8_t* k_pages, int8_t* v_pages, float* k_scales, float* v_scales,
+                     const int32_t* page_table, int max_pages_per_seq,
+                     const int32_t* context_lens, const int32_t* block_lens, int num_seqs,
+                     int num_kv_heads, int head_dim, int page_size, int num_pages,
+                     int* device_status, struct CUstream_st* stream);
+
+/*
+ * splash_verify_attention_workspace_size — bytes of device workspace that
+ * splash_verify_attention needs for these bounds on the current device
+ * (depends on its SM count). Returns 0 for invalid arguments.
+ */
+size_t splash_verify_attention_workspace_size(int num_seqs, int num_q_tokens, int num_q_heads,
+                                              int num_kv_heads, int head_dim, int max_block_len);
+
+/*
+ * splash_verify_attention — block-causal attention of every verify token over
+ * its sequence's int8 paged cache (the block itself already appended).
+ *
+ * Verify token t of sequence b, query head hq (KV head h = hq / G) attends to
+ * logical keys j = 0 .. context_lens[b] + t inclusive, dequantised as
+ * code * scale:
+ *   score_j = sm_scale * sum_d q[d] * k_hat_j[d]
+ *   out     = sum_j softmax(score)_j * v_hat_j              -> bf16 (RNE)
+ *   lse     = ln sum_j exp(score_j)   (sm_scale included)   -> fp32
+ * q, out: bf16 bit patterns [num_q_tokens, Hq, D]; lse: fp32 [num_q_tokens, Hq].
+ * num_q_tokens = sum(block_lens). max_block_len bounds every T_b (T_b * G must
+ * be <= 128). The KV range of every sequence is split across CTAs; partials
+ * are merged by log-sum-exp in `workspace` (>= the size query's bytes, 256-byte
+ * aligned). Deterministic: a fixed input, device and argument list gives
+ * bitwise identical outputs, independent of the physical page numbering.
+ */
+int splash_verify_attention(const uint16_t* q, int num_q_tokens,
+                            const int8_t* k_pages, const int8_t* v_pages,
+                            const float* k_scales, const float* v_scales,
+                            const int32_t* page_table, int max_pages_per_seq,
+                            const int32_t* context_lens, const int32_t* block_lens, int num_seqs,
+                            int num_q_heads, int num_kv_heads, int head_dim, int page_size,
+                            int num_pages, int max_block_len, float sm_scale,
+                            uint16_t* out, float* lse, void* workspace, size_t workspace_bytes,
+                            int* device_status, struct CUstream_st* stream);
+
+/*
+ * splash_verify_attention_tuned — splash_verify_attention with the kernel
+ * choice and the split granularity fixed by the caller (tests, benchmarks).
+ *   path: 0 automatic; 1 CUDA-core kernel for every sequence; 2 tensor-core
+ *         kernel for every sequence.
+ *   ctas_per_class: 0 automatic (fills the GPU); n > 0 uses n persistent CTAs
+ *         per kernel (1 = every sequence's KV range handled unsplit).
+ * Same result contract as splash_verify_attention (within rounding across
+ * different choices; bitwise for a fixed choice).
+ */
+int splash_verify_attention_tuned(const uint16_t* q, int num_q_tokens,
+                                  const int8_t* k_pages, const int8_t* v_pages,
+                                  const float* k_scales, const float* v_scales,
+                                  const int32_t* page_table, int max_pages_per_seq,
+                                  const int32_t* context_lens, const int32_t* block_lens,
+                                  int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                  int page_size, int num_pages, int max_block_len, float sm_scale,
+                                  uint16_t* out, float* lse, void* workspace,
+                                  size_t workspace_bytes, int* device_status,
+                                  struct CUstream_st* stream, int path, int ctas_per_class);
+
+/*
+ * splash_verify_attention_profiled — splash_verify_attention_tuned that also
+ * records two caller-created CUDA events on `stream`: `attn_begin` just before
+ * the attention kernel launch(es) and `attn_end` just after, so that the
+ * attention kernels can be timed apart from the split planner and the
+ * log-sum-exp combine. Either event may be NULL. Same work, same results.
+ */
+struct CUevent_st; /* cudaEvent_t */
+int splash_verify_attention_profiled(const uint16_t* q, int num_q_tokens,
+                                     const int8_t* k_pages, const int8_t* v_pages,
+                                     const float* k_scales, const float* v_scales,
+                                     const int32_t* page_table, int max_pages_per_seq,
+                                     const int32_t* context_lens, const int32_t* block_lens,
+                                     int num_seqs, int num_q_heads, int num_kv_heads,
+                                     int head_dim, int page_size, int num_pages,
+                                     int max_block_len, float sm_scale, uint16_t* out, float* lse,
+                                     void* workspace, size_t workspace_bytes, int* device_status,
+                                     struct CUstream_st* stream, int path, int ctas_per_class,
+                                     struct CUevent_st* attn_begin, struct CUevent_st* attn_end);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPLASH_KV_H */

@@ -1,0 +1,122 @@
+// Shared device/host definitions of the int8 paged-KV verify-attention library.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/splash_kv.h"
+
+namespace splash {
+
+constexpr int kPageSize = 16;
+constexpr int kClassTensor = 0;   // sequences whose T*G rows go to the tensor-core kernel
+constexpr int kClassSimt = 1;     // sequences whose rows go to the CUDA-core kernel
+constexpr int kNumClasses = 2;
+constexpr int kMaxRows = 128;     // T*G limit per sequence and KV head
+
+// Plan written by the planner kernel at the start of the workspace.
+struct PlanHeader {
+  int total_tiles[kNumClasses];   // key tiles of all (seq, KV head) units of a class
+  int ncta[kNumClasses];          // persistent CTAs the class's kernel is launched with
+  int tile_keys[kNumClasses];     // keys per tile
+  int num_seqs;
+  int num_kv_heads;
+  int group;                      // G = Hq / Hkv
+  int total_part_rows;            // partial rows the split units use
+  int rows_bound;                 // capacity of the partial buffers (rows)
+  int pad_[5];
+};
+static_assert(sizeof(PlanHeader) == 64, "header size");
+
+// Byte offsets of the workspace regions (all 256-aligned).
+struct WorkspaceLayout {
+  size_t q_off;        // int32 [B+1]   first token row of each sequence
+  size_t seq_T;        // int32 [B]     validated block length (0 if skipped)
+  size_t seq_ctx;      // int32 [B]
+  size_t seq_class;    // int32 [B]     kClassTensor / kClassSimt / -1
+  size_t stp;          // int32 [2][B+1] per-class exclusive prefix of tiles per sequence
+  size_t nseg;         // int32 [B*Hkv] CTAs (segments) that cover the unit
+  size_t cfirst;       // int32 [B*Hkv] first CTA of the unit
+  size_t part_base;    // int32 [B*Hkv] first partial row of the unit
+  size_t o_part;       // fp32  [rows_bound, D]
+  size_t lse_part;     // fp32  [rows_bound]
+  size_t total;
+};
+
+__host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+__host__ __device__ inline WorkspaceLayout make_layout(int B, int Hkv, int D, long long rows_bound) {
+  WorkspaceLayout L;
+  size_t o = align256(sizeof(PlanHeader));
+  L.q_off = o;      o = align256(o + sizeof(int) * (size_t)(B + 1));
+  L.seq_T = o;      o = align256(o + sizeof(int) * (size_t)B);
+  L.seq_ctx = o;    o = align256(o + sizeof(int) * (size_t)B);
+  L.seq_class = o;  o = align256(o + sizeof(int) * (size_t)B);
+  L.stp = o;        o = align256(o + sizeof(int) * (size_t)kNumClasses * (B + 1));
+  L.nseg = o;       o = align256(o + sizeof(int) * (size_t)B * Hkv);
+  L.cfirst = o;     o = align256(o + sizeof(int) * (size_t)B * Hkv);
+  L.part_base = o;  o = align256(o + sizeof(int) * (size_t)B * Hkv);
+  L.o_part = o;     o = align256(o + sizeof(float) * (size_t)rows_bound * D);
+  L.lse_part = o;   o = align256(o + sizeof(float) * (size_t)rows_bound);
+  L.total = o;
+  return L;
+}
+
+// Split of a class's tile stream over its persistent CTAs: CTA c owns tiles
+// [tile_begin(c), tile_begin(c+1)).
+__host__ __device__ inline int tile_begin(int c, int total, int ncta) {
+  return (int)(((long long)c * total) / ncta);
+}
+// The CTA whose range contains tile t (0 <= t < total).
+__host__ __device__ inline int cta_of_tile(int t, int total, int ncta) {
+  return (int)((((long long)t + 1) * ncta - 1) / total);
+}
+
+struct AttnParams {
+  const __nv_bfloat16* q;
+  const int8_t* k_pages;
+  const int8_t* v_pages;
+  const float* k_scales;
+  const float* v_scales;
+  const int32_t* page_table;
+  int max_pages_per_seq;
+  int num_seqs;
+  int num_q_heads;
+  int num_kv_heads;
+  int group;
+  int head_dim;
+  int num_pages;
+  float sm_scale_log2;            // sm_scale * log2(e)
+  __nv_bfloat16* out;
+  float* lse;
+  unsigned char* ws;
+  int* device_status;
+};
+
+__device__ inline void report(int* status, int code) {
+  if (status) atomicCAS(status, 0, code);
+}
+
+__device__ inline float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ inline float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Largest index i in [0, n] with a[i] <= x, for a non-decreasing array a[0..n].
+__device__ inline int upper_index(const int* a, int n, int x) {
+  int lo = 0, hi = n;
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if (a[mid] <= x) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+}  // namespace splash

@@ -1,0 +1,245 @@
+// Split plan and log-sum-exp combine of split-KV verify attention.
+//
+// Work unit = (sequence b, KV head h): its T_b*G query rows against keys
+// 0 .. ctx_b + T_b - 1. Each unit is cut into key tiles; the tiles of all units
+// of one class (tensor-core or CUDA-core kernel) form one stream that is split
+// evenly over that kernel's persistent CTAs. A unit touched by one CTA is
+// finished by it; a unit touched by n > 1 CTAs leaves n partials (o_i
+// normalised by its own sum, lse_i) that lse_combine merges:
+//   lse = ln sum_i exp(lse_i),  O = sum_i exp(lse_i - lse) o_i
+// (an empty partial has lse_i = -inf and weight 0).
+#include "splash_common.cuh"
+
+namespace splash {
+
+constexpr int kPlanThreads = 1024;
+
+// Exclusive scan over the CTA (kPlanThreads threads); *total receives the sum.
+__device__ inline int block_exclusive_scan(int v, int* s_warp, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) s_warp[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int x = s_warp[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    s_warp[lane] = x;
+  }
+  __syncthreads();
+  const int res = (warp ? s_warp[warp - 1] : 0) + incl - v;
+  *total = s_warp[31];
+  __syncthreads();
+  return res;
+}
+
+__global__ void __launch_bounds__(kPlanThreads)
+plan_kernel(const int32_t* __restrict__ context_lens, const int32_t* __restrict__ block_lens,
+            int num_seqs, int num_kv_heads, int group, int max_pages, int max_block_len,
+            int tile_tc, int tile_simt, int ncta_tc, int ncta_simt, int path, int rows_bound,
+            int num_q_tokens, unsigned char* ws, int* device_status) {
+  __shared__ int s_warp[32];
+  const WorkspaceLayout L = make_layout(num_seqs, num_kv_heads, 0, rows_bound);
+  int* q_off = reinterpret_cast<int*>(ws + L.q_off);
+  int* seq_T = reinterpret_cast<int*>(ws + L.seq_T);
+  int* seq_ctx = reinterpret_cast<int*>(ws + L.seq_ctx);
+  int* seq_class = reinterpret_cast<int*>(ws + L.seq_class);
+  int* stp = reinterpret_cast<int*>(ws + L.stp);
+  int* nseg = reinterpret_cast<int*>(ws + L.nseg);
+  int* cfirst = reinterpret_cast<int*>(ws + L.cfirst);
+  int* part_base = reinterpret_cast<int*>(ws + L.part_base);
+  const int tile[kNumClasses] = {tile_tc, tile_simt};
+  const int ncta[kNumClasses] = {ncta_tc, ncta_simt};
+
+  // pass 1: per sequence — validate, classify, prefix sums of rows and tiles
+  int run_q = 0, run_t0 = 0, run_t1 = 0;
+  for (int base = 0; base < num_seqs; base += kPlanThreads) {
+    const int b = base + threadIdx.x;
+    int T = 0, ctx = 0, cls = -1, tiles = 0;
+    if (b < num_seqs) {
+      T = block_lens[b];
+      ctx = context_lens[b];
+      const bool ok = T >= 0 && ctx >= 0 && T <= max_block_len &&
+                      (long long)ctx + T <= (long long)max_pages * kPageSize;
+      if (!ok) {
+        report(device_status, SPLASH_DEVICE_BAD_LENGTH);
+        T = 0;
+        ctx = 0;
+      }
+      if (T > 0) {
+        const int rows = T * group;
+        cls = path == 1 ? kClassSimt : path == 2 ? kClassTensor
+                        : (rows >= 16 ? kClassTensor : kClassSimt);
+        tiles = (ctx + T + tile[cls] - 1) / tile[cls];
+      }
+      seq_T[b] = T;
+      seq_ctx[b] = ctx;
+      seq_class[b] = cls;
+    }
+    int tot;
+    const int qo = block_exclusive_scan(T, s_warp, &tot);
+    if (b < num_seqs) q_off[b] = run_q + qo;
+    run_q += tot;
+    const int t0 = block_exclusive_scan(cls == 0 ? tiles * num_kv_heads : 0, s_warp, &tot);
+    if (b < num_seqs) stp[b] = run_t0 + t0;
+    run_t0 += tot;
+    const int t1 = block_exclusive_scan(cls == 1 ? tiles * num_kv_heads : 0, s_warp, &tot);
+    if (b < num_seqs) stp[(num_seqs + 1) + b] = run_t1 + t1;
+    run_t1 += tot;
+  }
+  if (threadIdx.x == 0) {
+    q_off[num_seqs] = run_q;
+    stp[num_seqs] = run_t0;
+    stp[(num_seqs + 1) + num_seqs] = run_t1;
+  }
+  __syncthreads();
+  // block lengths that sum past the q / out rows the caller passed: do nothing
+  const bool rows_ok = run_q <= num_q_tokens;
+  if (!rows_ok) {
+    if (threadIdx.x == 0) report(device_status, SPLASH_DEVICE_BAD_LENGTH);
+    run_t0 = run_t1 = 0;
+    for (int b = threadIdx.x; b < num_seqs; b += kPlanThreads) seq_class[b] = -1;
+    __syncthreads();
+  }
+  const int total[kNumClasses] = {run_t0, run_t1};
+
+  // pass 2: per unit (b, h) — segments and partial rows
+  const int num_units = num_seqs * num_kv_heads;
+  int run_rows = 0;
+  for (int base = 0; base < num_units; base += kPlanThreads) {
+    const int u = base + threadIdx.x;
+    int rows = 0;
+    if (u < num_units) {
+      const int b = u / num_kv_heads, h = u % num_kv_heads;
+      const int cls = seq_class[b];
+      int ns = 0, cf = 0;
+      if (cls >= 0) {
+        const int T = seq_T[b], ctx = seq_ctx[b];
+        const int tiles = (ctx + T + tile[cls] - 1) / tile[cls];
+        const int tp = stp[cls * (num_seqs + 1) + b] + h * tiles;
+        cf = cta_of_tile(tp, total[cls], ncta[cls]);
+        const int cl = cta_of_tile(tp + tiles - 1, total[cls], ncta[cls]);
+        ns = cl - cf + 1;
+        if (ns > 1) rows = ns * T * group;
+      }
+      nseg[u] = ns;
+      cfirst[u] = cf;
+    }
+    int tot;
+    const int pb = block_exclusive_scan(rows, s_warp, &tot);
+    if (u < num_units) part_base[u] = run_rows + pb;
+    run_rows += tot;
+  }
+  if (threadIdx.x == 0) {
+    PlanHeader* hd = reinterpret_cast<PlanHeader*>(ws);
+    hd->total_tiles[0] = run_t0;
+    hd->total_tiles[1] = run_t1;
+    hd->ncta[0] = ncta_tc;
+    hd->ncta[1] = ncta_simt;
+    hd->tile_keys[0] = tile_tc;
+    hd->tile_keys[1] = tile_simt;
+    hd->num_seqs = num_seqs;
+    hd->num_kv_heads = num_kv_heads;
+    hd->group = group;
+    hd->total_part_rows = run_rows;
+    hd->rows_bound = rows_bound;
+  }
+}
+
+// One warp per (token row, query head) of a split unit.
+template <int D>
+__global__ void __launch_bounds__(256)
+lse_combine_kernel(int num_q_tokens, int num_q_heads, int num_seqs, int num_kv_heads, int group,
+                   int rows_bound, const unsigned char* __restrict__ ws,
+                   __nv_bfloat16* __restrict__ out, float* __restrict__ lse_out) {
+  constexpr int EPL = D / 32;
+  const WorkspaceLayout L = make_layout(num_seqs, num_kv_heads, D, rows_bound);
+  const int* q_off = reinterpret_cast<const int*>(ws + L.q_off);
+  const int* seq_T = reinterpret_cast<const int*>(ws + L.seq_T);
+  const int* nseg = reinterpret_cast<const int*>(ws + L.nseg);
+  const int* part_base = reinterpret_cast<const int*>(ws + L.part_base);
+  const float* o_part = reinterpret_cast<const float*>(ws + L.o_part);
+  const float* lse_part = reinterpret_cast<const float*>(ws + L.lse_part);
+  const int lane = threadIdx.x & 31;
+  const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (row >= (long long)num_q_tokens * num_q_heads) return;
+  const int i = (int)(row / num_q_heads), hq = (int)(row % num_q_heads);
+  const int b = upper_index(q_off, num_seqs - 1, i);
+  const int h = hq / group, g = hq % group;
+  const int u = b * num_kv_heads + h;
+  const int n = nseg[u];
+  if (n <= 1 || i - q_off[b] >= seq_T[b]) return;
+  const int R = seq_T[b] * group;
+  const int r = (i - q_off[b]) * group + g;
+  const long long base = part_base[u];
+
+  float m = -INFINITY;
+  for (int j = lane; j < n; j += 32) m = fmaxf(m, lse_part[base + (long long)j * R + r]);
+  m = warp_max(m);
+  float acc[EPL];
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
+  float wsum = 0.f;
+  for (int j = 0; j < n; ++j) {
+    const long long pr = base + (long long)j * R + r;
+    const float lj = lse_part[pr];
+    const float w = (lj == -INFINITY) ? 0.f : __expf(lj - m);
+    wsum += w;
+    if (w != 0.f) {
+      const float* src = o_part + pr * D + lane * EPL;
+#pragma unroll
+      for (int e = 0; e < EPL; e += 2) {
+        const float2 v = *reinterpret_cast<const float2*>(src + e);
+        acc[e] = fmaf(w, v.x, acc[e]);
+        acc[e + 1] = fmaf(w, v.y, acc[e + 1]);
+      }
+    }
+  }
+  const float inv = 1.f / wsum;
+  __nv_bfloat16* dst = out + ((long long)i * num_q_heads + hq) * D + lane * EPL;
+#pragma unroll
+  for (int e = 0; e < EPL; e += 2)
+    *reinterpret_cast<__nv_bfloat162*>(dst + e) = __floats2bfloat162_rn(acc[e] * inv, acc[e + 1] * inv);
+  if (lane == 0) lse_out[(long long)i * num_q_heads + hq] = m + logf(wsum);
+}
+
+cudaError_t launch_plan(const int32_t* context_lens, const int32_t* block_lens, int num_seqs,
+                        int num_kv_heads, int group, int max_pages, int max_block_len, int tile_tc,
+                        int tile_simt, int ncta_tc, int ncta_simt, int path, int rows_bound,
+                        int num_q_tokens, unsigned char* ws, int* device_status,
+                        cudaStream_t stream) {
+  plan_kernel<<<1, kPlanThreads, 0, stream>>>(context_lens, block_lens, num_seqs, num_kv_heads,
+                                              group, max_pages, max_block_len, tile_tc, tile_simt,
+                                              ncta_tc, ncta_simt, path, rows_bound, num_q_tokens,
+                                              ws, device_status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(int num_q_tokens, int num_q_heads, int num_seqs, int num_kv_heads,
+                           int group, int head_dim, int rows_bound, const unsigned char* ws,
+                           __nv_bfloat16* out, float* lse, cudaStream_t stream) {
+  const long long rows = (long long)num_q_tokens * num_q_heads;
+  if (rows == 0) return cudaSuccess;
+  const int grid = (int)((rows + 7) / 8);
+#define SPLASH_COMBINE(DD)                                                                     \
+  lse_combine_kernel<DD><<<grid, 256, 0, stream>>>(num_q_tokens, num_q_heads, num_seqs,       \
+                                                   num_kv_heads, group, rows_bound, ws, out, lse)
+  switch (head_dim) {
+    case 64: SPLASH_COMBINE(64); break;
+    case 128: SPLASH_COMBINE(128); break;
+    case 256: SPLASH_COMBINE(256); break;
+    default: return cudaErrorInvalidValue;
+  }
+#undef SPLASH_COMBINE
+  return cudaGetLastError();
+}
+
+}  // namespace splash

@@ -1,0 +1,102 @@
+"""Host-only checks of the C ABI: the library builds, loads and exports every
+symbol the header declares; argument errors come back before any launch."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "splash_kv.h")
+
+
+@pytest.fixture(scope="module")
+def sk():
+    from speculative_verify_attention_kv_gb300 import build
+    if not os.path.exists(build.LIB):
+        build.build()
+    from speculative_verify_attention_kv_gb300 import splash_kv
+    return splash_kv
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(splash_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("splash_kv_append", "splash_verify_attention",
+              "splash_verify_attention_workspace_size", "splash_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(sk):
+    lib = ctypes.CDLL(sk._LIB_PATH)
+    for n in declared_functions():
+        assert hasattr(lib, n), n
+    assert set(declared_functions()) <= set(sk.EXPORTED) | {"splash_abi_version"}
+
+
+def test_status_strings(sk):
+    assert sk.status_string(0) == "SPLASH_OK"
+    assert sk.status_string(-1) == "SPLASH_ERR_INVALID_ARGUMENT"
+    assert sk.status_string(-2) == "SPLASH_ERR_UNSUPPORTED"
+    assert sk.status_string(-3) == "SPLASH_ERR_WORKSPACE_TOO_SMALL"
+    assert sk.status_string(-4) == "SPLASH_ERR_CUDA"
+    assert sk.status_string(12345) == "SPLASH_UNKNOWN_STATUS"
+    assert sk.LIB.splash_abi_version() == 1
+
+
+FAKE = ctypes.c_void_p(256)  # never dereferenced: validation fails first
+
+
+def _append(sk, **kw):
+    a = dict(k=FAKE, v=FAKE, n=4, kp=FAKE, vp=FAKE, ks=FAKE, vs=FAKE, tab=FAKE, maxp=4,
+             ctx=FAKE, T=FAKE, B=1, hkv=2, D=128, P=16, pages=8, st=None, stream=None)
+    a.update(kw)
+    return sk.LIB.splash_kv_append(a["k"], a["v"], a["n"], a["kp"], a["vp"], a["ks"], a["vs"],
+                                   a["tab"], a["maxp"], a["ctx"], a["T"], a["B"], a["hkv"],
+                                   a["D"], a["P"], a["pages"], a["st"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(P=8), -2), (dict(D=96), -2), (dict(D=512), -2), (dict(hkv=0), -1), (dict(n=-1), -1),
+    (dict(B=-2), -1), (dict(maxp=0), -1), (dict(k=None), -1), (dict(tab=None), -1),
+    (dict(vs=None), -1), (dict(n=0), 0), (dict(B=0), 0),
+])
+def test_kv_append_argument_errors(sk, kw, code):
+    assert _append(sk, **kw) == code
+
+
+def _attn(sk, **kw):
+    a = dict(q=FAKE, n=4, kp=FAKE, vp=FAKE, ks=FAKE, vs=FAKE, tab=FAKE, maxp=4, ctx=FAKE,
+             T=FAKE, B=1, hq=8, hkv=2, D=128, P=16, pages=8, maxT=4, sm=0.088, out=FAKE,
+             lse=FAKE, ws=FAKE, wsb=1 << 30, st=None, stream=None, path=0, ctas=0)
+    a.update(kw)
+    args = [a[k] for k in ("q", "n", "kp", "vp", "ks", "vs", "tab", "maxp", "ctx", "T", "B", "hq",
+                           "hkv", "D", "P", "pages", "maxT", "sm", "out", "lse", "ws", "wsb",
+                           "st", "stream")]
+    return sk.LIB.splash_verify_attention_tuned(*args, a["path"], a["ctas"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(hq=7), -1), (dict(hkv=0), -1), (dict(D=100), -2), (dict(P=32), -2),
+    (dict(maxT=40), -2),              # T*G = 160 > 128 rows
+    (dict(maxT=-1), -1), (dict(n=-3), -1), (dict(maxp=0), -1), (dict(path=3), -1),
+    (dict(ctas=-1), -1), (dict(q=None), -1), (dict(ws=None), -1), (dict(lse=None), -1),
+    (dict(ws=ctypes.c_void_p(256 + 16)), -1),   # workspace not 256-byte aligned
+    (dict(n=0), 0), (dict(B=0), 0),
+])
+def test_verify_attention_argument_errors(sk, kw, code):
+    assert _attn(sk, **kw) == code
+
+
+def test_workspace_query_rejects_bad_shapes(sk):
+    f = sk.LIB.splash_verify_attention_workspace_size
+    assert f(1, 4, 7, 2, 128, 4) == 0
+    assert f(1, 4, 8, 2, 100, 4) == 0
+    assert f(1, 4, 8, 2, 128, 64) == 0

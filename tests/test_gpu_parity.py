@@ -1,0 +1,293 @@
+"""GPU parity of the CUDA path against the fp64 oracle (through the C ABI).
+
+Bars: int8 codes and fp32 scales bit-exact; attention O (bf16) within max-abs
+1e-2 and mean-abs 1e-3 of the fp64 oracle, LSE within 1e-3 absolute.
+"""
+from __future__ import annotations
+
+import functools
+
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+from oracle import splash_oracle as O  # noqa: E402
+from speculative_verify_attention_kv_gb300 import build as _build  # noqa: E402
+
+import os  # noqa: E402
+if not os.path.exists(_build.LIB):
+    _build.build()
+
+from speculative_verify_attention_kv_gb300 import splash_kv as sk  # noqa: E402
+from speculative_verify_attention_kv_gb300 import workloads as wl  # noqa: E402
+
+from common import oracle_pool, q_values  # noqa: E402
+from gpu_common import Run, assert_parity, compare  # noqa: E402
+
+
+def oracle_attention(W, pool, seqs=None):
+    return O.attention(q_values(W), pool, W.page_table, W.context_lens, W.block_lens,
+                       W.spec.num_kv_heads, float(W.sm_scale), seqs=seqs)
+
+
+def seq_rows(W, seqs):
+    return np.concatenate([np.arange(W.q_offsets[b], W.q_offsets[b + 1]) for b in seqs]).astype(np.int64)
+
+
+@functools.lru_cache(maxsize=None)
+def _tc_probe():
+    W = wl.custom(8, 2, 128, [20], [4], seed=1)
+    r = Run(W)
+    r.append_block()
+    try:
+        r.attend(path=sk.PATH_TENSOR)
+    except sk.SplashError as e:
+        if e.status == -2:
+            return False
+        raise
+    return True
+
+
+PATHS = [sk.PATH_AUTO, sk.PATH_SIMT, sk.PATH_TENSOR]
+
+
+def _path_ok(path):
+    return path != sk.PATH_TENSOR or _tc_probe()
+
+
+# ---------------------------------------------------------------------------
+# kv_append: bit-exact codes and scales
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("D", [64, 128, 256])
+def test_kv_append_bit_exact_edge_rows(D):
+    rng = np.random.default_rng(D)
+    n, hkv = 40, 2
+    x = rng.standard_normal((n, hkv, D)).astype(np.float32)
+    x[0] = 0
+    x[1, 0, :] = 0
+    x[1, 0, 5] = np.float32(-2.0 ** -140)
+    x[2, 1, :] = 0
+    x[2, 1, :4] = np.float32(190 * 2.0 ** -149)
+    x[3, 0, :8] = np.array([127.0, 2.5, 3.5, -2.5, 0.5, 126.5, -127.0, 1.5], np.float32)
+    x[3, 0, 8:] = 0
+    x[4:10, :, 3] *= 8
+    x[10] *= np.float32(1e-30)
+    W = wl.custom(2 * hkv, hkv, D, [0, 7], [17, n - 17], seed=2)
+    pool = sk.alloc_pool(W.num_pages, hkv, D)
+    table = torch.from_numpy(W.page_table).cuda()
+    sk.splash_kv_append(torch.from_numpy(x).cuda(), torch.from_numpy(-x).cuda(), *pool, table,
+                        torch.from_numpy(W.context_lens).cuda(), torch.from_numpy(W.block_lens).cuda())
+    torch.cuda.synchronize()
+    opool = O.PagedPool(W.num_pages, hkv, 16, D)
+    O.kv_append(opool, x, -x, W.page_table, W.context_lens, W.block_lens)
+    kp, vp, ks, vs = [t.cpu().numpy() for t in pool]
+    assert np.array_equal(kp, opool.k_codes) and np.array_equal(vp, opool.v_codes)
+    assert np.array_equal(ks.view(np.uint32), opool.k_scales.view(np.uint32))
+    assert np.array_equal(vs.view(np.uint32), opool.v_scales.view(np.uint32))
+
+
+# ---------------------------------------------------------------------------
+# attention: small cases, full oracle
+# ---------------------------------------------------------------------------
+SMALL = [
+    dict(hq=8, hkv=2, D=128, ctx=[37, 200, 0], T=[4, 1, 3]),
+    dict(hq=24, hkv=4, D=256, ctx=[130, 513, 1000], T=[16, 1, 8]),
+    dict(hq=4, hkv=4, D=64, ctx=[700], T=[5]),
+    dict(hq=24, hkv=4, D=256, ctx=[300, 300], T=[16, 16], prefix=256),
+    dict(hq=32, hkv=4, D=128, ctx=[333], T=[16]),          # T*G = 128 rows
+    dict(hq=24, hkv=4, D=256, ctx=[50, 60, 70], T=[3, 0, 2]),   # an idle sequence
+    dict(hq=24, hkv=4, D=256, ctx=[4000], T=[4]),
+]
+
+
+@pytest.mark.parametrize("case", range(len(SMALL)))
+@pytest.mark.parametrize("path", PATHS)
+def test_attention_small_cases(case, path):
+    c = SMALL[case]
+    if not _path_ok(path):
+        pytest.skip("tensor-core kernel not built for this head_dim")
+    W = wl.custom(c["hq"], c["hkv"], c["D"], c["ctx"], c["T"], seed=20 + case,
+                  shared_prefix_len=c.get("prefix", 0))
+    r = Run(W)
+    r.append_block()
+    o_ref, l_ref = oracle_attention(W, oracle_pool(W))
+    for ctas in (0, 1, 3):
+        o, l = r.attend(path=path, ctas=ctas)
+        torch.cuda.synchronize()
+        assert_parity(o, l, o_ref, l_ref, what=f"case {case} path {path} ctas {ctas}")
+    assert int(r.status.item()) == 0
+
+
+# ---------------------------------------------------------------------------
+# the five workloads at full size, sampled sequences
+# ---------------------------------------------------------------------------
+SAMPLES = {"tiny": None, "single_32k": [0], "shared_prefix": [0, 3],
+           "batch16_32k": [0, 9], "ragged64": "pick"}
+
+
+def _ragged_pick(W):
+    T = W.block_lens
+    ctx = W.context_lens
+    picks = {int(np.argmax(ctx)), int(np.argmin(ctx))}
+    for t in (1, 4, 8, 16):
+        idx = np.where(T == t)[0]
+        if len(idx):
+            picks.add(int(idx[np.argmin(ctx[idx])]))
+    return sorted(picks)
+
+
+@pytest.mark.parametrize("name", list(SAMPLES))
+def test_workload_parity_sampled(name):
+    W = wl.make(name)
+    seqs = SAMPLES[name]
+    if seqs == "pick":
+        seqs = _ragged_pick(W)
+    if seqs is None:
+        seqs = list(range(W.num_seqs))
+    r = Run(W, seqs=seqs)
+    r.append_block()
+    o, l = r.attend()
+    torch.cuda.synchronize()
+    opool = oracle_pool(W, seqs)
+    # codes of every page the sampled sequences use are bit-exact
+    kp, vp, ks, vs = r.pool
+    pages = np.unique(np.concatenate([W.page_table[b][W.page_table[b] >= 0] for b in seqs]))
+    pg = torch.from_numpy(pages).cuda().long()
+    assert np.array_equal(kp[pg].cpu().numpy(), opool.k_codes[pages])
+    assert np.array_equal(vp[pg].cpu().numpy(), opool.v_codes[pages])
+    Lb = {b: int(W.context_lens[b] + W.block_lens[b]) for b in seqs}
+    ks_h, vs_h = ks[pg].cpu().numpy(), vs[pg].cpu().numpy()
+    for b in seqs:   # scales of used slots (tail slots keep their poison)
+        for j in range(0, Lb[b], 997):
+            pi = int(np.searchsorted(pages, W.page_table[b][j // 16]))
+            assert ks_h[pi, :, j % 16].view(np.uint32).tolist() == \
+                opool.k_scales[pages[pi], :, j % 16].view(np.uint32).tolist()
+            assert vs_h[pi, :, j % 16].view(np.uint32).tolist() == \
+                opool.v_scales[pages[pi], :, j % 16].view(np.uint32).tolist()
+    o_ref, l_ref = oracle_attention(W, opool, seqs)
+    rows = seq_rows(W, seqs)
+    assert_parity(o, l, o_ref, l_ref, rows=rows, what=name)
+    assert int(r.status.item()) == 0
+
+
+# ---------------------------------------------------------------------------
+# properties
+# ---------------------------------------------------------------------------
+def _small_run(seed=5, ctx=(900, 37, 2100), T=(16, 1, 8)):
+    W = wl.custom(24, 4, 256, list(ctx), list(T), seed=seed)
+    r = Run(W)
+    r.append_block()
+    return W, r
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_deterministic_and_page_permutation_bitwise(path):
+    if not _path_ok(path):
+        pytest.skip("tensor-core kernel not built")
+    W, r = _small_run()
+    o1, l1 = [t.clone() for t in r.attend(path=path)]
+    o2, l2 = [t.clone() for t in r.attend(path=path)]
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    perm = torch.from_numpy(np.random.default_rng(3).permutation(W.num_pages)).cuda().long()
+    newpool = []
+    for t in r.pool:
+        n = torch.empty_like(t)
+        n[perm] = t
+        newpool.append(n)
+    r.pool = tuple(newpool)
+    tab = r.table.long()
+    r.table = torch.where(tab >= 0, perm[tab.clamp(min=0)], tab).int().contiguous()
+    o3, l3 = r.attend(path=path)
+    assert torch.equal(o1, o3) and torch.equal(l1, l3)
+
+
+def test_split_and_unsplit_agree():
+    W, r = _small_run()
+    o_ref, l_ref = oracle_attention(W, oracle_pool(W))
+    outs = []
+    for ctas in (1, 2, 7, 0):
+        o, l = [t.clone() for t in r.attend(ctas=ctas)]
+        assert_parity(o, l, o_ref, l_ref, what=f"ctas={ctas}")
+        outs.append((o.float(), l))
+    for o, l in outs[1:]:
+        assert (o - outs[0][0]).abs().max().item() <= 2 ** -7
+        assert (l - outs[0][1]).abs().max().item() <= 1e-4
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_future_block_keys_do_not_leak(path):
+    if not _path_ok(path):
+        pytest.skip("tensor-core kernel not built")
+    W, r = _small_run(ctx=(500,), T=(8,))
+    o1, l1 = [t.clone() for t in r.attend(path=path)]
+    kp, vp, ks, vs = r.pool
+    for j in range(500 + 4, 508):   # poison block tokens 4..7
+        page, slot = int(W.page_table[0, j // 16]), j % 16
+        kp[page, :, slot] = 127
+        vp[page, :, slot] = -127
+        vs[page, :, slot] = 1e4
+    o2, l2 = r.attend(path=path)
+    assert torch.equal(o1[:4], o2[:4]) and torch.equal(l1[:4], l2[:4])
+    assert not torch.equal(o1[4:], o2[4:])
+
+
+def test_t1_rows_are_plain_decode():
+    W = wl.custom(24, 4, 256, [777, 1500], [1, 1], seed=31)
+    r = Run(W)
+    r.append_block()
+    o, l = r.attend()
+    opool = oracle_pool(W)
+    q = q_values(W)
+    for b in range(2):
+        n = int(W.context_lens[b]) + 1
+        for h in range(4):
+            k, v = O.gather_keys(opool, W.page_table[b], h, n)
+            qq = torch.tensor(q[b, 6 * h:6 * h + 6])
+            ref = torch.softmax(float(W.sm_scale) * qq @ torch.tensor(k).T, -1) @ torch.tensor(v)
+            err = (o[b, 6 * h:6 * h + 6].float().cpu().double() - ref).abs().max().item()
+            assert err <= 1e-2
+
+
+def test_bad_page_sets_device_status():
+    W, r = _small_run(ctx=(300,), T=(4,))
+    tab = r.table.clone()
+    tab[0, 5] = W.num_pages + 3
+    r.table = tab
+    r.status.zero_()
+    r.attend()
+    torch.cuda.synchronize()
+    assert int(r.status.item()) == sk.DEVICE_BAD_PAGE
+    r.status.zero_()
+    r.table = tab
+    r.append_block()       # block positions 300..303 live on page 18: valid -> no error
+    torch.cuda.synchronize()
+    assert int(r.status.item()) == 0
+
+
+def test_bad_length_sets_device_status():
+    W, r = _small_run(ctx=(300,), T=(4,))
+    r.ctx = torch.tensor([W.max_pages_per_seq * 16], dtype=torch.int32, device="cuda")
+    r.status.zero_()
+    r.attend()
+    torch.cuda.synchronize()
+    assert int(r.status.item()) == sk.DEVICE_BAD_LENGTH
+
+
+def test_workspace_too_small():
+    W, r = _small_run(ctx=(300,), T=(4,))
+    r.ws = r.ws[:1024]
+    with pytest.raises(sk.SplashError) as e:
+        r.attend()
+    assert e.value.status == -3
+
+
+def test_empty_batch_is_a_no_op():
+    W = wl.custom(8, 2, 128, [10], [0], seed=3)
+    r = Run(W)
+    r.attend()
+    torch.cuda.synchronize()
