@@ -18,7 +18,8 @@ constexpr int kMaxRows = 128;     // T*G limit per sequence and KV head
 // Plan written by the planner kernel at the start of the workspace.
 struct PlanHeader {
   int total_tiles[kNumClasses];   // key tiles of all (seq, KV head) units of a class
-  int ncta[kNumClasses];          // persistent CTAs the class's kernel is launched with
+  int ncta[kNumClasses];          // CTAs of the class's kernel that own tiles: min(launched, tiles);
+                                  // CTAs with blockIdx.x >= ncta exit at once
   int tile_keys[kNumClasses];     // keys per tile
   int num_seqs;
   int num_kv_heads;

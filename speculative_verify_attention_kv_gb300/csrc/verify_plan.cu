@@ -110,6 +110,10 @@ plan_kernel(const int32_t* __restrict__ context_lens, const int32_t* __restrict_
     __syncthreads();
   }
   const int total[kNumClasses] = {run_t0, run_t1};
+  // a class's kernel uses at most one CTA per tile, so that every CTA it uses
+  // owns >= 1 tile and the CTAs covering a unit are consecutive, all non-empty
+  int ncta_eff[kNumClasses];
+  for (int c = 0; c < kNumClasses; ++c) ncta_eff[c] = min(ncta[c], total[c]);
 
   // pass 2: per unit (b, h) — segments and partial rows
   const int num_units = num_seqs * num_kv_heads;
@@ -125,8 +129,8 @@ plan_kernel(const int32_t* __restrict__ context_lens, const int32_t* __restrict_
         const int T = seq_T[b], ctx = seq_ctx[b];
         const int tiles = (ctx + T + tile[cls] - 1) / tile[cls];
         const int tp = stp[cls * (num_seqs + 1) + b] + h * tiles;
-        cf = cta_of_tile(tp, total[cls], ncta[cls]);
-        const int cl = cta_of_tile(tp + tiles - 1, total[cls], ncta[cls]);
+        cf = cta_of_tile(tp, total[cls], ncta_eff[cls]);
+        const int cl = cta_of_tile(tp + tiles - 1, total[cls], ncta_eff[cls]);
         ns = cl - cf + 1;
         if (ns > 1) rows = ns * T * group;
       }
@@ -142,8 +146,8 @@ plan_kernel(const int32_t* __restrict__ context_lens, const int32_t* __restrict_
     PlanHeader* hd = reinterpret_cast<PlanHeader*>(ws);
     hd->total_tiles[0] = run_t0;
     hd->total_tiles[1] = run_t1;
-    hd->ncta[0] = ncta_tc;
-    hd->ncta[1] = ncta_simt;
+    hd->ncta[0] = ncta_eff[0];
+    hd->ncta[1] = ncta_eff[1];
     hd->tile_keys[0] = tile_tc;
     hd->tile_keys[1] = tile_simt;
     hd->num_seqs = num_seqs;

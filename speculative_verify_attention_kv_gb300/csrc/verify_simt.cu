@@ -59,7 +59,8 @@ verify_simt_kernel(AttnParams p, int rows_cap) {
   float* lse_part = reinterpret_cast<float*>(p.ws + L.lse_part);
 
   const int total = hd->total_tiles[kClassSimt];
-  const int ncta = gridDim.x;
+  const int ncta = hd->ncta[kClassSimt];
+  if ((int)blockIdx.x >= ncta) return;
   int t = tile_begin(blockIdx.x, total, ncta);
   const int t_end = tile_begin(blockIdx.x + 1, total, ncta);
 
