@@ -35,6 +35,16 @@ def oracle_attention(W, pool, seqs=None):
                        W.spec.num_kv_heads, float(W.sm_scale), seqs=seqs)
 
 
+def written_slots(W, seqs):
+    """(page, slot) of every logical position 0..ctx+T-1 of the listed sequences."""
+    pages, slots = [], []
+    for b in seqs:
+        j = np.arange(int(W.context_lens[b] + W.block_lens[b]))
+        pages.append(W.page_table[b][j // 16].astype(np.int64))
+        slots.append(j % 16)
+    return np.concatenate(pages), np.concatenate(slots)
+
+
 def seq_rows(W, seqs):
     return np.concatenate([np.arange(W.q_offsets[b], W.q_offsets[b + 1]) for b in seqs]).astype(np.int64)
 
@@ -154,21 +164,17 @@ def test_workload_parity_sampled(name):
     o, l = r.attend()
     torch.cuda.synchronize()
     opool = oracle_pool(W, seqs)
-    # codes of every page the sampled sequences use are bit-exact
+    # every written slot of the sampled sequences: codes and scales bit-exact
+    # (the unwritten tail slots keep their poison)
+    pg, sl = written_slots(W, seqs)
+    pg_t, sl_t = torch.from_numpy(pg).cuda(), torch.from_numpy(sl).cuda()
     kp, vp, ks, vs = r.pool
-    pages = np.unique(np.concatenate([W.page_table[b][W.page_table[b] >= 0] for b in seqs]))
-    pg = torch.from_numpy(pages).cuda().long()
-    assert np.array_equal(kp[pg].cpu().numpy(), opool.k_codes[pages])
-    assert np.array_equal(vp[pg].cpu().numpy(), opool.v_codes[pages])
-    Lb = {b: int(W.context_lens[b] + W.block_lens[b]) for b in seqs}
-    ks_h, vs_h = ks[pg].cpu().numpy(), vs[pg].cpu().numpy()
-    for b in seqs:   # scales of used slots (tail slots keep their poison)
-        for j in range(0, Lb[b], 997):
-            pi = int(np.searchsorted(pages, W.page_table[b][j // 16]))
-            assert ks_h[pi, :, j % 16].view(np.uint32).tolist() == \
-                opool.k_scales[pages[pi], :, j % 16].view(np.uint32).tolist()
-            assert vs_h[pi, :, j % 16].view(np.uint32).tolist() == \
-                opool.v_scales[pages[pi], :, j % 16].view(np.uint32).tolist()
+    assert np.array_equal(kp[pg_t, :, sl_t].cpu().numpy(), opool.k_codes[pg, :, sl])
+    assert np.array_equal(vp[pg_t, :, sl_t].cpu().numpy(), opool.v_codes[pg, :, sl])
+    assert np.array_equal(ks[pg_t, :, sl_t].cpu().numpy().view(np.uint32),
+                          opool.k_scales[pg, :, sl].view(np.uint32))
+    assert np.array_equal(vs[pg_t, :, sl_t].cpu().numpy().view(np.uint32),
+                          opool.v_scales[pg, :, sl].view(np.uint32))
     o_ref, l_ref = oracle_attention(W, opool, seqs)
     rows = seq_rows(W, seqs)
     assert_parity(o, l, o_ref, l_ref, rows=rows, what=name)
