@@ -66,8 +66,11 @@ enum {
 
 enum {
   SPLASH_DEVICE_BAD_PAGE = 1,         /* page id < 0 or >= num_pages where a page is needed */
-  SPLASH_DEVICE_BAD_LENGTH = 2        /* ctx or T negative, T > max_block_len, or
-                                         ctx + T > max_pages_per_seq * P */
+  SPLASH_DEVICE_BAD_LENGTH = 2,       /* ctx or T negative, T > max_block_len, or
+                                         ctx + T > max_pages_per_seq * P, or
+                                         sum(block_lens) > num_q_tokens */
+  SPLASH_DEVICE_TIMEOUT = 3           /* an internal wait of the tensor-core kernel gave
+                                         up after ~1 s (outputs of that call undefined) */
 };
 
 /* Human-readable name of a SPLASH_* status (static string, never NULL). */
@@ -122,7 +125,7 @@ size_t splash_verify_attention_workspace_size(int num_seqs, int num_q_tokens, in
  *   lse     = ln sum_j exp(score_j)   (sm_scale included)   -> fp32
  * q, out: bf16 bit patterns [num_q_tokens, Hq, D]; lse: fp32 [num_q_tokens, Hq].
  * num_q_tokens = sum(block_lens). max_block_len bounds every T_b (T_b * G must
- * be <= 128). The KV range of every sequence is split across CTAs; partials
+ * be <= 128). sm_scale must be finite and > 0. The KV range of every sequence is split across CTAs; partials
  * are merged by log-sum-exp in `workspace` (>= the size query's bytes, 256-byte
  * aligned). Deterministic: a fixed input, device and argument list gives
  * bitwise identical outputs, independent of the physical page numbering.

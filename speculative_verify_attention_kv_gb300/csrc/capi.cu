@@ -17,7 +17,7 @@ size_t simt_smem_bytes(int, int);
 cudaError_t launch_verify_tc(const AttnParams&, int, int, cudaStream_t);
 bool tc_supported(int head_dim);
 constexpr int kSimtTile = 64;
-constexpr int kTcTile = 128;
+constexpr int kTcTile = 64;
 
 namespace {
 
@@ -125,10 +125,9 @@ size_t splash_verify_attention_workspace_size(int num_seqs, int num_q_tokens, in
     return 0;
   const int sms = device_sm_count();
   if (sms <= 0) return 0;
-  int nt, ns;
-  default_ctas(sms, head_dim, max_block_len * (num_q_heads / num_kv_heads), &nt, &ns);
+  // the largest CTA counts any automatic choice can make
   return workspace_bytes_for(num_seqs, num_q_tokens, num_q_heads, num_kv_heads, head_dim,
-                             max_block_len, nt, ns);
+                             max_block_len, sms, 4 * sms);
 }
 
 int splash_verify_attention_profiled(
@@ -152,19 +151,20 @@ int splash_verify_attention_profiled(
   const int G = num_q_heads / num_kv_heads;
   const int rows_cap = max_block_len * G;
   if (rows_cap == 0) return SPLASH_OK;
+  if (!(sm_scale > 0.f) || sm_scale == INFINITY) return SPLASH_ERR_INVALID_ARGUMENT;
   const bool tc_ok = tc_supported(head_dim);
   if (path == 2 && !tc_ok) return SPLASH_ERR_UNSUPPORTED;
   if (!tc_ok) path = 1;
-  const size_t simt_smem = simt_smem_bytes(head_dim, rows_cap);
+  // rows the CUDA-core kernel may see: all (path 1), none (path 2), < 16 (automatic)
+  const int rows_simt = path == 1 ? rows_cap : path == 2 ? 0 : (rows_cap < 15 ? rows_cap : 15);
   // the CUDA-core kernel holds every row of a unit in shared memory
-  const bool simt_fits = simt_smem <= 227 * 1024;
-  if (path == 1 && !simt_fits) return SPLASH_ERR_UNSUPPORTED;
-  if (path == 0 && !simt_fits && !tc_ok) return SPLASH_ERR_UNSUPPORTED;
+  if (rows_simt > 0 && simt_smem_bytes(head_dim, rows_simt) > 227 * 1024)
+    return SPLASH_ERR_UNSUPPORTED;
 
   const int sms = device_sm_count();
   if (sms <= 0) return SPLASH_ERR_CUDA;
   int nt, ns;
-  default_ctas(sms, head_dim, rows_cap, &nt, &ns);
+  default_ctas(sms, head_dim, rows_simt > 0 ? rows_simt : 1, &nt, &ns);
   if (ctas_per_class > 0) nt = ns = ctas_per_class;
   const size_t need = workspace_bytes_for(num_seqs, num_q_tokens, num_q_heads, num_kv_heads,
                                           head_dim, max_block_len, nt, ns);
@@ -206,7 +206,7 @@ int splash_verify_attention_profiled(
     if (e != cudaSuccess) return SPLASH_ERR_CUDA;
   }
   if (path != 2) {
-    e = launch_verify_simt(p, rows_cap, ns, s);
+    e = launch_verify_simt(p, rows_simt, ns, s);
     if (e != cudaSuccess) return SPLASH_ERR_CUDA;
   }
   if (attn_end && cudaEventRecord(reinterpret_cast<cudaEvent_t>(attn_end), s) != cudaSuccess)

@@ -66,8 +66,8 @@ def _tc_probe():
 PATHS = [sk.PATH_AUTO, sk.PATH_SIMT, sk.PATH_TENSOR]
 
 
-def _path_ok(path):
-    return path != sk.PATH_TENSOR or _tc_probe()
+def _path_ok(path, head_dim=256):
+    return path != sk.PATH_TENSOR or sk.tensor_path_available(head_dim)
 
 
 # ---------------------------------------------------------------------------
@@ -119,7 +119,7 @@ SMALL = [
 @pytest.mark.parametrize("path", PATHS)
 def test_attention_small_cases(case, path):
     c = SMALL[case]
-    if not _path_ok(path):
+    if not _path_ok(path, c["D"]):
         pytest.skip("tensor-core kernel not built for this head_dim")
     W = wl.custom(c["hq"], c["hkv"], c["D"], c["ctx"], c["T"], seed=20 + case,
                   shared_prefix_len=c.get("prefix", 0))
