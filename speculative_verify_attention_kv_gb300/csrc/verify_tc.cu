@@ -15,11 +15,14 @@
 // are exact in fp16). The K scale multiplies score columns, the V scale is
 // folded into P before P is rounded to fp16.
 //
-// Warp roles (416 threads):
+// Warp roles (448 threads):
 //   warps 0-3   softmax + epilogue: thread = TMEM lane = query row
-//   warps 4-11  loaders: 16-byte loads of int8 pages -> fp16 in registers ->
-//               128B-swizzled SMEM tiles (K: K-major, V: MN-major), scales
+//   warps 4-11  converters: int8 codes from the staging ring -> fp16 in
+//               registers -> 128B-swizzled SMEM tiles (K: K-major, V: MN-major)
 //   warp  12    TMEM allocation and the single MMA-issuing thread
+//   warp  13    producer: one thread issues bulk async copies (TMA, untiled)
+//               of whole (page, KV head) blocks of codes and scales into a
+//               2-stage staging ring ahead of the converters
 // Handshakes are mbarriers; every wait gives up after ~1 s, sets
 // SPLASH_DEVICE_TIMEOUT and lets the CTA drain and free its TMEM.
 #include "splash_common.cuh"
@@ -28,12 +31,15 @@ namespace splash {
 namespace tc {
 
 constexpr int kTileKeys = 64;
-constexpr int kStages = 2;
+constexpr int kPagesPerTile = kTileKeys / kPageSize;
+constexpr int kStages = 2;                    // S/P buffers in TMEM, fp16 K/V tiles, scales
+constexpr int kRing = 2;                      // int8 staging stages
 constexpr int kSoftmaxWarps = 4;
 constexpr int kLoadWarps = 8;
 constexpr int kLoadThreads = 32 * kLoadWarps;
-constexpr int kThreads = 32 * (kSoftmaxWarps + kLoadWarps + 1);
 constexpr int kMmaWarp = kSoftmaxWarps + kLoadWarps;
+constexpr int kProducerWarp = kMmaWarp + 1;
+constexpr int kThreads = 32 * (kProducerWarp + 1);
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.0f;          // lazy rescale threshold (factor 256)
 constexpr unsigned long long kWaitNs = 1000000000ull;
@@ -45,11 +51,15 @@ struct Cfg {
   static constexpr int kSCol = D / 2;                            // S[2]: 64 columns each
   static constexpr int kOCol = D / 2 + 2 * kTileKeys;            // O: D columns
   static_assert(kOCol + D <= (int)kTmemCols, "TMEM budget");
-  // dynamic shared memory: K[2], V[2] tiles, scales, barriers (+1 KB for alignment)
+  // staging ring stage: K codes [64][D], V codes [64][D], K scales [64], V scales [64]
+  static constexpr int kRingCodes = kTileKeys * D;
+  static constexpr int kRingStage = 2 * kRingCodes + 2 * kTileKeys * 4;
+  // dynamic shared memory: fp16 K tiles [2], fp16 V tiles [2], scales [2], ring, barriers
   static constexpr int kSmemTiles = 2 * kStages * kTileBytes;
   static constexpr int kSmemScales = 2 * kStages * kTileKeys * 4;
+  static constexpr int kSmemRing = kRing * kRingStage;
   // at least 120 KB so that one CTA (and its 512 TMEM columns) owns the SM
-  static constexpr int kSmemUsed = 1024 + kSmemTiles + kSmemScales + 256;
+  static constexpr int kSmemUsed = 1024 + kSmemTiles + kSmemScales + kSmemRing + 512;
   static constexpr int kSmemBytes = kSmemUsed > 120 * 1024 ? kSmemUsed : 120 * 1024;
 };
 
@@ -99,6 +109,11 @@ struct Sync {
   }
 };
 
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float y;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(y) : "f"(a), "f"(b), "f"(c));
+  return y;
+}
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -217,8 +232,11 @@ struct SegIter {
 };
 
 struct Smem {
+  uint64_t ring_full[kRing];
+  uint64_t ring_empty[kRing];
   uint64_t kv_full[kStages];
-  uint64_t kv_empty[kStages];
+  uint64_t v_free[kStages];
+  uint64_t k_free[kStages];
   uint64_t s_full[kStages];
   uint64_t p_full[kStages];
   uint64_t o_done;
@@ -226,93 +244,80 @@ struct Smem {
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
+  int ring_valid[kRing];          // bit j: page j of the staged tile was copied
 };
 
-// loader registers for one tile: 4*D/256 chunks of 16 B of K and of V, scales
-template <int D>
-struct LoadRegs {
-  uint4 k[4 * D / kLoadThreads];
-  uint4 v[4 * D / kLoadThreads];
-  float sk, sv;
-  int key0;
-};
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
 
+// Producer: stage the int8 codes and fp32 scales of tile `it` of segment s.
+// *valid_mask receives the mask of pages copied (pages past the sequence end or with an
+// invalid id are skipped; their stale staging bytes are finite codes whose
+// scales the converters zero).
 template <int D>
-__device__ __forceinline__ void load_tile(const AttnParams& p, const Seg& s, int it, int lt,
-                                          LoadRegs<D>& r) {
-  constexpr int kPer = 4 * D / kLoadThreads;
+__device__ __forceinline__ void stage_tile(const AttnParams& p, const Seg& s, int it,
+                                           uint8_t* stage, uint32_t bar, int* valid_mask) {
+  using C = Cfg<D>;
   const int k0 = it * kTileKeys;
   const int32_t* ptab = p.page_table + (size_t)s.b * p.max_pages_per_seq;
-  r.key0 = k0;
+  int mask = 0, pages[kPagesPerTile];
 #pragma unroll
-  for (int q = 0; q < kPer; ++q) {
-    const int c = q * kLoadThreads + lt;          // 16-byte chunk of the tile
-    const int j = c / D;                          // page of the tile
-    const int off = (c % D) * 16;                 // byte in the (page, head) block
-    uint4 kk = make_uint4(0, 0, 0, 0), vv = make_uint4(0, 0, 0, 0);
-    if (k0 + 16 * j < s.Lk) {
-      const int page = ptab[(k0 >> 4) + j];
+  for (int j = 0; j < kPagesPerTile; ++j) {
+    pages[j] = -1;
+    if (k0 + kPageSize * j < s.Lk) {
+      const int page = ptab[(k0 / kPageSize) + j];
       if (page >= 0 && page < p.num_pages) {
-        const size_t base = ((size_t)page * p.num_kv_heads + s.h) * (kPageSize * D) + off;
-        kk = __ldg(reinterpret_cast<const uint4*>(p.k_pages + base));
-        vv = __ldg(reinterpret_cast<const uint4*>(p.v_pages + base));
-      }
-    }
-    r.k[q] = kk;
-    r.v[q] = vv;
-  }
-  r.sk = 0.f;
-  r.sv = 0.f;
-  if (lt < kTileKeys) {
-    const int key = k0 + lt;
-    if (key < s.Lk) {
-      const int page = ptab[key >> 4];
-      if (page >= 0 && page < p.num_pages) {
-        const size_t si = ((size_t)page * p.num_kv_heads + s.h) * kPageSize + (key & 15);
-        r.sk = __ldg(p.k_scales + si);
-        r.sv = __ldg(p.v_scales + si);
+        pages[j] = page;
+        mask |= 1 << j;
       } else {
         report(p.device_status, SPLASH_DEVICE_BAD_PAGE);
       }
     }
   }
+  constexpr uint32_t kBlock = kPageSize * D;          // codes of one (page, head)
+  constexpr uint32_t kScaleBlock = kPageSize * 4;
+  *valid_mask = mask;   // published by the release of the arrive below
+  mbar_expect_tx(bar, (uint32_t)__popc(mask) * (2 * kBlock + 2 * kScaleBlock));
+  const uint32_t sbase = smem_u32(stage);
+#pragma unroll
+  for (int j = 0; j < kPagesPerTile; ++j) {
+    if (pages[j] < 0) continue;
+    const size_t blk = (size_t)pages[j] * p.num_kv_heads + s.h;
+    bulk_g2s(sbase + j * kBlock, p.k_pages + blk * kBlock, kBlock, bar);
+    bulk_g2s(sbase + C::kRingCodes + j * kBlock, p.v_pages + blk * kBlock, kBlock, bar);
+    bulk_g2s(sbase + 2 * C::kRingCodes + j * kScaleBlock, p.k_scales + blk * kPageSize,
+             kScaleBlock, bar);
+    bulk_g2s(sbase + 2 * C::kRingCodes + kTileKeys * 4 + j * kScaleBlock,
+             p.v_scales + blk * kPageSize, kScaleBlock, bar);
+  }
 }
 
-// fp16 tile element (key n, d) lives at block d/64, row n, 16-byte chunk
-// ((d%64)/8) ^ (n%8) of that 128-byte row (SWIZZLE_128B, 1024-byte atoms)
+// Converters: 8 consecutive codes (one key, channels d0..d0+7) per unit; the
+// 8 threads of a quarter warp cover one 128-byte swizzled row, so the 16-byte
+// stores are free of bank conflicts. fp16 element (key n, d) lives at block
+// d/64, row n, 16-byte chunk ((d%64)/8) ^ (n%8) (SWIZZLE_128B, 1024-byte atoms).
 template <int D>
-__device__ __forceinline__ void store_tile(const LoadRegs<D>& r, int lt, uint8_t* kbuf,
-                                           uint8_t* vbuf, float* ks, float* vs) {
-  constexpr int kPer = 4 * D / kLoadThreads;
+__device__ __forceinline__ void convert_codes(const uint8_t* src, uint8_t* dst, int lt) {
+  constexpr int kUnits = kTileKeys * D / 8;
 #pragma unroll
-  for (int q = 0; q < kPer; ++q) {
-    const int c = q * kLoadThreads + lt;
-    const int j = c / D;
-    const int off = (c % D) * 16;
-    const int n = 16 * j + off / D;               // key within the tile
-    const int d0 = off % D;                       // first of 16 channels
-    const int blk = d0 / 64;
-    const int c16 = (d0 % 64) / 8;
-    const uint32_t row = blk * (kTileKeys * 128) + n * 128;
-    const uint32_t a0 = row + (((c16) ^ (n & 7)) << 4);
-    const uint32_t a1 = row + (((c16 + 1) ^ (n & 7)) << 4);
-    uint4 h0, h1;
-    i8x4_to_h2x2(r.k[q].x, h0.x, h0.y);
-    i8x4_to_h2x2(r.k[q].y, h0.z, h0.w);
-    i8x4_to_h2x2(r.k[q].z, h1.x, h1.y);
-    i8x4_to_h2x2(r.k[q].w, h1.z, h1.w);
-    *reinterpret_cast<uint4*>(kbuf + a0) = h0;
-    *reinterpret_cast<uint4*>(kbuf + a1) = h1;
-    i8x4_to_h2x2(r.v[q].x, h0.x, h0.y);
-    i8x4_to_h2x2(r.v[q].y, h0.z, h0.w);
-    i8x4_to_h2x2(r.v[q].z, h1.x, h1.y);
-    i8x4_to_h2x2(r.v[q].w, h1.z, h1.w);
-    *reinterpret_cast<uint4*>(vbuf + a0) = h0;
-    *reinterpret_cast<uint4*>(vbuf + a1) = h1;
-  }
-  if (lt < kTileKeys) {
-    ks[lt] = r.sk;
-    vs[lt] = r.sv;
+  for (int q = 0; q < kUnits / kLoadThreads; ++q) {
+    const int u = q * kLoadThreads + lt;
+    const int n = u / (D / 8), c8 = u % (D / 8);
+    const uint2 w = *reinterpret_cast<const uint2*>(src + n * D + c8 * 8);
+    uint4 h;
+    i8x4_to_h2x2(w.x, h.x, h.y);
+    i8x4_to_h2x2(w.y, h.z, h.w);
+    const uint32_t a = (c8 / 8) * (kTileKeys * 128) + n * 128 + (((c8 & 7) ^ (n & 7)) << 4);
+    *reinterpret_cast<uint4*>(dst + a) = h;
   }
 }
 
@@ -323,11 +328,12 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  uint8_t* kbuf = smem;                                   // [kStages][tile]
-  uint8_t* vbuf = smem + kStages * C::kTileBytes;         // [kStages][tile]
+  uint8_t* kbuf = smem;                                   // [kStages] fp16 K tiles
+  uint8_t* vbuf = smem + kStages * C::kTileBytes;         // [kStages] fp16 V tiles
   float* kscale = reinterpret_cast<float*>(smem + C::kSmemTiles);   // [kStages][64]
   float* vscale = kscale + kStages * kTileKeys;                     // [kStages][64]
-  Smem* sh = reinterpret_cast<Smem*>(smem + C::kSmemTiles + C::kSmemScales);
+  uint8_t* ring = smem + C::kSmemTiles + C::kSmemScales;            // [kRing][stage]
+  Smem* sh = reinterpret_cast<Smem*>(ring + C::kSmemRing);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int B = p.num_seqs, Hkv = p.num_kv_heads, G = p.group;
@@ -348,9 +354,14 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
   if ((int)blockIdx.x >= ncta) return;
 
   if (tid == 0) {
+    for (int s = 0; s < kRing; ++s) {
+      mbar_init(smem_u32(&sh->ring_full[s]), 1);
+      mbar_init(smem_u32(&sh->ring_empty[s]), kLoadThreads);
+    }
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&sh->kv_full[s]), kLoadThreads);
-      mbar_init(smem_u32(&sh->kv_empty[s]), 1);
+      mbar_init(smem_u32(&sh->v_free[s]), 1);
+      mbar_init(smem_u32(&sh->k_free[s]), 1);
       mbar_init(smem_u32(&sh->s_full[s]), 1);
       mbar_init(smem_u32(&sh->p_full[s]), 32 * kSoftmaxWarps);
     }
@@ -443,21 +454,34 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
         float alpha = 1.f;
         if (warp_live) {
           const int k0 = it * kTileKeys;
-          const float* ks = kscale + st * kTileKeys;
-          const float* vs = vscale + st * kTileKeys;
+          const float4* ks4 = reinterpret_cast<const float4*>(kscale + st * kTileKeys);
+          const float4* vs4 = reinterpret_cast<const float4*>(vscale + st * kTileKeys);
           uint32_t s0[32], s1[32];
           tmem_ld32(tmem + lane_base + C::kSCol + st * kTileKeys, s0);
           tmem_ld32(tmem + lane_base + C::kSCol + st * kTileKeys + 32, s1);
           tmem_wait_ld();
-          float x[64];
-          float mt = -INFINITY;
-          const int nvis = row_live ? min(kTileKeys, lim - k0 + 1) : 0;   // visible keys in tile
+          // x = S * sK (packed fp32x2), masked columns -> -inf
+          float2 x[32];
 #pragma unroll
-          for (int j = 0; j < 64; ++j) {
-            const float sj = __uint_as_float(j < 32 ? s0[j] : s1[j - 32]);
-            x[j] = (j < nvis) ? sj * ks[j] : -INFINITY;
-            mt = fmaxf(mt, x[j]);
+          for (int j4 = 0; j4 < 16; ++j4) {
+            const float4 kq = ks4[j4];
+            const uint32_t* src = j4 < 8 ? &s0[4 * j4] : &s1[4 * j4 - 32];
+            x[2 * j4] = __fmul2_rn(make_float2(__uint_as_float(src[0]), __uint_as_float(src[1])),
+                                   make_float2(kq.x, kq.y));
+            x[2 * j4 + 1] = __fmul2_rn(make_float2(__uint_as_float(src[2]), __uint_as_float(src[3])),
+                                       make_float2(kq.z, kq.w));
           }
+          const int nvis = row_live ? min(kTileKeys, lim - k0 + 1) : 0;   // visible keys in tile
+          if (nvis < kTileKeys) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              if (2 * j >= nvis) x[j].x = -INFINITY;
+              if (2 * j + 1 >= nvis) x[j].y = -INFINITY;
+            }
+          }
+          float mt = -INFINITY;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) mt = fmax3(mt, x[j].x, x[j].y);
           const float m_new = fmaxf(m, mt);
           float m_use = m;
           if (m == -INFINITY) {
@@ -468,32 +492,38 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
           }
           m = m_use;
           const float base = (m_use == -INFINITY) ? 0.f : rowfac * m_use;
-          float sum = 0.f;
+          const float2 rf2 = make_float2(rowfac, rowfac), nb2 = make_float2(-base, -base);
+          float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
-          for (int j = 0; j < 64; j += 2) {
-            const float p0 = (j < nvis) ? ex2(fmaf(rowfac, x[j], -base)) : 0.f;
-            const float p1 = (j + 1 < nvis) ? ex2(fmaf(rowfac, x[j + 1], -base)) : 0.f;
-            sum += p0 + p1;
-            __half2 hv = __floats2half2_rn(p0 * vs[j], p1 * vs[j + 1]);
-            pw[j / 2] = *reinterpret_cast<uint32_t*>(&hv);
+          for (int j4 = 0; j4 < 16; ++j4) {
+            const float4 vq = vs4[j4];
+            const float2 e0 = __ffma2_rn(x[2 * j4], rf2, nb2);
+            const float2 e1 = __ffma2_rn(x[2 * j4 + 1], rf2, nb2);
+            const float2 p0 = make_float2(ex2(e0.x), ex2(e0.y));
+            const float2 p1 = make_float2(ex2(e1.x), ex2(e1.y));
+            acc = __fadd2_rn(acc, __fadd2_rn(p0, p1));
+            const float2 q0 = __fmul2_rn(p0, make_float2(vq.x, vq.y));
+            const float2 q1 = __fmul2_rn(p1, make_float2(vq.z, vq.w));
+            __half2 h0 = __float22half2_rn(q0), h1 = __float22half2_rn(q1);
+            pw[2 * j4] = *reinterpret_cast<uint32_t*>(&h0);
+            pw[2 * j4 + 1] = *reinterpret_cast<uint32_t*>(&h1);
           }
-          l = l * alpha + sum;
+          l = l * alpha + (acc.x + acc.y);
         }
-        // PV of the previous tile has to be complete before O is rescaled
-        if (it > s.i0) {
+        // a rescale of O waits for the previous tile's PV (rare: the running
+        // max is only moved when it grows by more than 2^8)
+        if (it > s.i0 && warp_live && __any_sync(0xffffffffu, alpha != 1.f)) {
           ok = sync.wait(smem_u32(&sh->o_done), (g - 1) & 1);
           if (!ok) break;
           fence_after();
-          if (warp_live && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
-            for (int c0 = 0; c0 < D; c0 += 32) {
-              uint32_t v[32];
-              tmem_ld32(tmem + lane_base + C::kOCol + c0, v);
-              tmem_wait_ld();
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t v[32];
+            tmem_ld32(tmem + lane_base + C::kOCol + c0, v);
+            tmem_wait_ld();
 #pragma unroll
-              for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * alpha);
-              tmem_st32(tmem + lane_base + C::kOCol + c0, v);
-            }
+            for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * alpha);
+            tmem_st32(tmem + lane_base + C::kOCol + c0, v);
           }
         }
         if (warp_live) {
@@ -555,42 +585,54 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
       ++nsegs;
     }
   } else if (warp < kSoftmaxWarps + kLoadWarps) {
-    // ============================================================== loaders
+    // =========================================================== converters
     const int lt = tid - 32 * kSoftmaxWarps;
     int g = 0;
     Seg s;
-    bool have = iter.next(s);
-    int it = have ? s.i0 : 0;
-    LoadRegs<D> ra, rb;
-    if (have) load_tile<D>(p, s, it, lt, ra);
     bool ok = true;
-    auto step = [&](LoadRegs<D>& cur, LoadRegs<D>& nxt) -> bool {
-      // advance to the next tile and prefetch it
-      Seg s2 = s;
-      int it2 = it + 1;
-      bool have2 = true;
-      if (it2 >= s.i1) {
-        have2 = iter.next(s2);
-        it2 = have2 ? s2.i0 : 0;
+    while (ok && iter.next(s)) {
+      for (int it = s.i0; it < s.i1; ++it, ++g) {
+        const int r = g % kRing, st = g % kStages;
+        ok = sync.wait(smem_u32(&sh->ring_full[r]), (g / kRing) & 1);
+        if (!ok) break;
+        const uint8_t* stage = ring + r * C::kRingStage;
+        const uint32_t free_par = ((g / kStages) & 1) ^ 1;
+        ok = sync.wait(smem_u32(&sh->k_free[st]), free_par);
+        if (!ok) break;
+        convert_codes<D>(stage, kbuf + st * C::kTileBytes, lt);
+        ok = sync.wait(smem_u32(&sh->v_free[st]), free_par);
+        if (!ok) break;
+        convert_codes<D>(stage + C::kRingCodes, vbuf + st * C::kTileBytes, lt);
+        if (lt < 2 * kTileKeys) {
+          const int n = lt % kTileKeys;
+          const int key = it * kTileKeys + n;
+          const bool valid = key < s.Lk && ((sh->ring_valid[r] >> (n / kPageSize)) & 1);
+          const float* src = reinterpret_cast<const float*>(stage + 2 * C::kRingCodes);
+          if (lt < kTileKeys) kscale[st * kTileKeys + n] = valid ? src[n] : 0.f;
+          else vscale[st * kTileKeys + n] = valid ? src[kTileKeys + n] : 0.f;
+        }
+        fence_async_smem();
+        mbar_arrive(smem_u32(&sh->kv_full[st]));
+        mbar_arrive(smem_u32(&sh->ring_empty[r]));
       }
-      if (have2) load_tile<D>(p, s2, it2, lt, nxt);
-      const int st = g % kStages;
-      if (!sync.wait(smem_u32(&sh->kv_empty[st]), ((g / kStages) & 1) ^ 1)) return false;
-      store_tile<D>(cur, lt, kbuf + st * C::kTileBytes, vbuf + st * C::kTileBytes,
-                    kscale + st * kTileKeys, vscale + st * kTileKeys);
-      fence_async_smem();
-      mbar_arrive(smem_u32(&sh->kv_full[st]));
-      ++g;
-      s = s2;
-      it = it2;
-      have = have2;
-      return true;
-    };
-    while (have && ok) {
-      ok = step(ra, rb);
-      if (!have || !ok) break;
-      ok = step(rb, ra);
     }
+  } else if (warp == kProducerWarp) {
+    // ============================================================ producer
+    if (lane == 0) {
+      int g = 0;
+      Seg s;
+      bool ok = true;
+      while (ok && iter.next(s)) {
+        for (int it = s.i0; it < s.i1; ++it, ++g) {
+          const int r = g % kRing;
+          ok = sync.wait(smem_u32(&sh->ring_empty[r]), ((g / kRing) & 1) ^ 1);
+          if (!ok) break;
+          stage_tile<D>(p, s, it, ring + r * C::kRingStage, smem_u32(&sh->ring_full[r]),
+                        &sh->ring_valid[r]);
+        }
+      }
+    }
+    __syncwarp();
   } else {
     // ================================================================= MMA
     if (lane == 0) {
@@ -604,41 +646,63 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
         if (!ok) break;
         fence_after();
         const int n = s.i1 - s.i0;
-        auto issue_qk = [&](int gi) -> bool {
-          const int st = gi % kStages;
-          if (!sync.wait(smem_u32(&sh->kv_full[st]), (gi / kStages) & 1)) return false;
-          fence_after();
-          const uint32_t kaddr = smem_u32(kbuf + st * C::kTileBytes);
+        // QK(i) and PV(i) are issued in their own orders, each as soon as its
+        // inputs are ready; QK(i) also needs PV(i-2) issued (S/P buffer reuse;
+        // MMAs run in issue order). In-flight limit: bounded by the same timeout.
+        int nq = 0, np = 0;
+        unsigned long long t_idle = 0;
+        while (np < n) {
+          bool progressed = false;
+          if (nq < n && nq <= np + 1) {
+            const int gi = g + nq, st = gi % kStages;
+            if (mbar_try_wait(smem_u32(&sh->kv_full[st]), (gi / kStages) & 1)) {
+              fence_after();
+              const uint32_t kaddr = smem_u32(kbuf + st * C::kTileBytes);
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint64_t bd = sdesc(kaddr + (kk / 4) * (kTileKeys * 128) + (kk % 4) * 32, 16, 1024);
-            mma_ts(tmem + C::kSCol + st * kTileKeys, tmem + C::kQCol + kk * 8, bd, kIdescQK,
-                   kk > 0);
+              for (int kk = 0; kk < D / 16; ++kk) {
+                const uint64_t bd =
+                    sdesc(kaddr + (kk / 4) * (kTileKeys * 128) + (kk % 4) * 32, 16, 1024);
+                mma_ts(tmem + C::kSCol + st * kTileKeys, tmem + C::kQCol + kk * 8, bd,
+                       kIdescQK, kk > 0);
+              }
+              mma_commit(smem_u32(&sh->s_full[st]));
+              mma_commit(smem_u32(&sh->k_free[st]));
+              ++nq;
+              progressed = true;
+            }
           }
-          mma_commit(smem_u32(&sh->s_full[st]));
-          return true;
-        };
-        auto issue_pv = [&](int gi, bool first) -> bool {
-          const int st = gi % kStages;
-          if (!sync.wait(smem_u32(&sh->p_full[st]), (gi / kStages) & 1)) return false;
-          fence_after();
-          const uint32_t vaddr = smem_u32(vbuf + st * C::kTileBytes);
+          if (np < nq) {
+            const int gi = g + np, st = gi % kStages;
+            if (mbar_try_wait(smem_u32(&sh->p_full[st]), (gi / kStages) & 1)) {
+              fence_after();
+              const uint32_t vaddr = smem_u32(vbuf + st * C::kTileBytes);
 #pragma unroll
-          for (int kk = 0; kk < kTileKeys / 16; ++kk) {
-            const uint64_t bd = sdesc(vaddr + kk * 16 * 128, kTileKeys * 128, 1024);
-            mma_ts(tmem + C::kOCol, tmem + C::kSCol + st * kTileKeys + kk * 8, bd, kIdescPV,
-                   (first && kk == 0) ? 0u : 1u);
+              for (int kk = 0; kk < kTileKeys / 16; ++kk) {
+                const uint64_t bd = sdesc(vaddr + kk * 16 * 128, kTileKeys * 128, 1024);
+                mma_ts(tmem + C::kOCol, tmem + C::kSCol + st * kTileKeys + kk * 8, bd,
+                       kIdescPV, (np == 0 && kk == 0) ? 0u : 1u);
+              }
+              mma_commit(smem_u32(&sh->v_free[st]));
+              mma_commit(smem_u32(&sh->o_done));
+              ++np;
+              progressed = true;
+            }
           }
-          mma_commit(smem_u32(&sh->kv_empty[st]));
-          mma_commit(smem_u32(&sh->o_done));
-          return true;
-        };
-        ok = issue_qk(g);
-        for (int i = 1; i < n && ok; ++i) {
-          ok = issue_qk(g + i);
-          if (ok) ok = issue_pv(g + i - 1, i == 1);
+          if (progressed) {
+            t_idle = 0;
+          } else {
+            if (sh->abort_flag) { ok = false; break; }
+            const unsigned long long now = global_ns();
+            if (t_idle == 0) {
+              t_idle = now;
+            } else if (now - t_idle > kWaitNs) {
+              sh->abort_flag = 1;
+              report(p.device_status, SPLASH_DEVICE_TIMEOUT);
+              ok = false;
+              break;
+            }
+          }
         }
-        if (ok) ok = issue_pv(g + n - 1, n == 1);
         g += n;
         ++nsegs;
       }
