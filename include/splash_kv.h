@@ -69,8 +69,10 @@ enum {
   SPLASH_DEVICE_BAD_LENGTH = 2,       /* ctx or T negative, T > max_block_len, or
                                          ctx + T > max_pages_per_seq * P, or
                                          sum(block_lens) > num_q_tokens */
-  SPLASH_DEVICE_TIMEOUT = 3           /* an internal wait of the tensor-core kernel gave
+  SPLASH_DEVICE_TIMEOUT = 3,          /* an internal wait of the tensor-core kernel gave
                                          up after ~1 s (outputs of that call undefined) */
+  SPLASH_DEVICE_INTERNAL = 4          /* the tensor-core kernel found its shared memory
+                                         misaligned and did nothing */
 };
 
 /* Human-readable name of a SPLASH_* status (static string, never NULL). */

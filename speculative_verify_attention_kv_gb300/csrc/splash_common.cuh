@@ -6,7 +6,7 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 
-#include "../../include/splash_kv.h"
+#include "splash_kv.h"
 
 namespace splash {
 

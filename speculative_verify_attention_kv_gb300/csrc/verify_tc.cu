@@ -20,9 +20,12 @@
 //   warps 4-11  converters: int8 codes from the staging ring -> fp16 in
 //               registers -> 128B-swizzled SMEM tiles (K: K-major, V: MN-major)
 //   warp  12    TMEM allocation and the single MMA-issuing thread
-//   warp  13    producer: one thread issues bulk async copies (TMA, untiled)
-//               of whole (page, KV head) blocks of codes and scales into a
-//               2-stage staging ring ahead of the converters
+//   warp  13    producer: bulk async copies (TMA, untiled) of whole
+//               (page, KV head) blocks: codes into a 2-stage int8 staging
+//               ring ahead of the converters, scales straight into the
+//               3-stage scale arrays the softmax reads
+// Buffers: fp16 K tiles x2 (free once QK of the tile is done), fp16 V tiles x3
+// (free once PV is done), so a slow stage does not stall the two behind it.
 // Handshakes are mbarriers; every wait gives up after ~1 s, sets
 // SPLASH_DEVICE_TIMEOUT and lets the CTA drain and free its TMEM.
 #include "splash_common.cuh"
@@ -32,7 +35,8 @@ namespace tc {
 
 constexpr int kTileKeys = 64;
 constexpr int kPagesPerTile = kTileKeys / kPageSize;
-constexpr int kStages = 2;                    // S/P buffers in TMEM, fp16 K/V tiles, scales
+constexpr int kStages = 2;                    // S/P buffers in TMEM, fp16 K tiles
+constexpr int kVStages = 3;                   // fp16 V tiles and the scale arrays
 constexpr int kRing = 2;                      // int8 staging stages
 constexpr int kSoftmaxWarps = 4;
 constexpr int kLoadWarps = 8;
@@ -51,16 +55,23 @@ struct Cfg {
   static constexpr int kSCol = D / 2;                            // S[2]: 64 columns each
   static constexpr int kOCol = D / 2 + 2 * kTileKeys;            // O: D columns
   static_assert(kOCol + D <= (int)kTmemCols, "TMEM budget");
-  // staging ring stage: K codes [64][D], V codes [64][D], K scales [64], V scales [64]
+  // staging ring stage: K codes [64][D], V codes [64][D]
   static constexpr int kRingCodes = kTileKeys * D;
-  static constexpr int kRingStage = 2 * kRingCodes + 2 * kTileKeys * 4;
-  // dynamic shared memory: fp16 K tiles [2], fp16 V tiles [2], scales [2], ring, barriers
-  static constexpr int kSmemTiles = 2 * kStages * kTileBytes;
-  static constexpr int kSmemScales = 2 * kStages * kTileKeys * 4;
-  static constexpr int kSmemRing = kRing * kRingStage;
-  // at least 120 KB so that one CTA (and its 512 TMEM columns) owns the SM
-  static constexpr int kSmemUsed = 1024 + kSmemTiles + kSmemScales + kSmemRing + 512;
-  static constexpr int kSmemBytes = kSmemUsed > 120 * 1024 ? kSmemUsed : 120 * 1024;
+  static constexpr int kRingStage = 2 * kRingCodes;
+  // dynamic shared memory (offsets from a 1024-byte aligned base)
+  static constexpr int kOffK = 0;                                        // fp16 K [2]
+  static constexpr int kOffV = kOffK + kStages * kTileBytes;             // fp16 V [3]
+  static constexpr int kOffRing = kOffV + kVStages * kTileBytes;         // int8 [2]
+  static constexpr int kOffScales = kOffRing + kRing * kRingStage;       // fp32 [3][2][64]
+  static constexpr int kOffBars = kOffScales + kVStages * 2 * kTileKeys * 4;
+  static constexpr int kBarBytes = 512;
+  static constexpr int kSmemUsed = kOffBars + kBarBytes;
+  // + up to 1 KB to align the base (the kernel checks the room it got); at
+  // least 120 KB so that one CTA (and its 512 TMEM columns) owns the SM
+  static constexpr int kSmemMax = 227 * 1024;
+  static constexpr int kSmemAligned = kSmemUsed + 1024 < kSmemMax ? kSmemUsed + 1024 : kSmemMax;
+  static constexpr int kSmemBytes = kSmemAligned > 120 * 1024 ? kSmemAligned : 120 * 1024;
+  static_assert(kSmemUsed <= kSmemMax, "shared memory budget");
 };
 
 // ---------------------------------------------------------------- PTX helpers
@@ -83,6 +94,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.b32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.b32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
       : "r"(bar), "r"(parity)
@@ -232,19 +255,20 @@ struct SegIter {
 };
 
 struct Smem {
-  uint64_t ring_full[kRing];
-  uint64_t ring_empty[kRing];
-  uint64_t kv_full[kStages];
-  uint64_t v_free[kStages];
-  uint64_t k_free[kStages];
-  uint64_t s_full[kStages];
-  uint64_t p_full[kStages];
-  uint64_t o_done;
-  uint64_t q_full;
+  uint64_t ring_full[kRing];      // producer tx -> converters
+  uint64_t ring_empty[kRing];     // converters -> producer
+  uint64_t sc_full[kVStages];     // producer tx (scales) -> softmax
+  uint64_t kv_full[kStages];      // converters -> MMA (fp16 K and V of the tile ready)
+  uint64_t k_free[kStages];       // QK done -> converters
+  uint64_t v_free[kVStages];      // PV done -> converters, producer (scales)
+  uint64_t s_full[kStages];       // QK done -> softmax
+  uint64_t p_full[kStages];       // softmax -> MMA
+  uint64_t p_free[kStages];       // PV of the buffer's tile done -> MMA (QK may
+                                  // overwrite the S/P buffer), softmax (O rescale, epilogue)
+  uint64_t q_full;                // softmax (Q' in TMEM) -> MMA
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
-  int ring_valid[kRing];          // bit j: page j of the staged tile was copied
 };
 
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
@@ -259,45 +283,50 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
       : "memory");
 }
 
-// Producer: stage the int8 codes and fp32 scales of tile `it` of segment s.
-// *valid_mask receives the mask of pages copied (pages past the sequence end or with an
-// invalid id are skipped; their stale staging bytes are finite codes whose
-// scales the converters zero).
+// Producer (one warp): stage tile `it` of segment s. Lanes 0..3 look up the
+// tile's page ids in parallel; lanes 0..15 issue one bulk copy each (page
+// j = lane/4: K codes, V codes into the ring stage; K scales, V scales into the
+// scale arrays). Pages past the sequence end or with an invalid id are
+// skipped: their stale codes are finite and the softmax gives their keys
+// probability 0 without reading their scales.
 template <int D>
 __device__ __forceinline__ void stage_tile(const AttnParams& p, const Seg& s, int it,
-                                           uint8_t* stage, uint32_t bar, int* valid_mask) {
+                                           uint8_t* stage, float* scales, uint32_t ring_bar,
+                                           uint32_t scale_bar, int lane) {
   using C = Cfg<D>;
   const int k0 = it * kTileKeys;
   const int32_t* ptab = p.page_table + (size_t)s.b * p.max_pages_per_seq;
-  int mask = 0, pages[kPagesPerTile];
-#pragma unroll
-  for (int j = 0; j < kPagesPerTile; ++j) {
-    pages[j] = -1;
-    if (k0 + kPageSize * j < s.Lk) {
-      const int page = ptab[(k0 / kPageSize) + j];
-      if (page >= 0 && page < p.num_pages) {
-        pages[j] = page;
-        mask |= 1 << j;
-      } else {
-        report(p.device_status, SPLASH_DEVICE_BAD_PAGE);
-      }
+  int page = -1;
+  if (lane < kPagesPerTile && k0 + kPageSize * lane < s.Lk) {
+    page = ptab[(k0 / kPageSize) + lane];
+    if (page < 0 || page >= p.num_pages) {
+      report(p.device_status, SPLASH_DEVICE_BAD_PAGE);
+      page = -1;
     }
   }
+  const int mask = (int)(__ballot_sync(0xffffffffu, page >= 0) & ((1u << kPagesPerTile) - 1));
   constexpr uint32_t kBlock = kPageSize * D;          // codes of one (page, head)
   constexpr uint32_t kScaleBlock = kPageSize * 4;
-  *valid_mask = mask;   // published by the release of the arrive below
-  mbar_expect_tx(bar, (uint32_t)__popc(mask) * (2 * kBlock + 2 * kScaleBlock));
-  const uint32_t sbase = smem_u32(stage);
-#pragma unroll
-  for (int j = 0; j < kPagesPerTile; ++j) {
-    if (pages[j] < 0) continue;
-    const size_t blk = (size_t)pages[j] * p.num_kv_heads + s.h;
-    bulk_g2s(sbase + j * kBlock, p.k_pages + blk * kBlock, kBlock, bar);
-    bulk_g2s(sbase + C::kRingCodes + j * kBlock, p.v_pages + blk * kBlock, kBlock, bar);
-    bulk_g2s(sbase + 2 * C::kRingCodes + j * kScaleBlock, p.k_scales + blk * kPageSize,
-             kScaleBlock, bar);
-    bulk_g2s(sbase + 2 * C::kRingCodes + kTileKeys * 4 + j * kScaleBlock,
-             p.v_scales + blk * kPageSize, kScaleBlock, bar);
+  if (lane == 0) {
+    mbar_expect_tx(ring_bar, (uint32_t)__popc(mask) * (2 * kBlock));
+    mbar_expect_tx(scale_bar, (uint32_t)__popc(mask) * (2 * kScaleBlock));
+  }
+  __syncwarp();
+  const int j = lane >> 2, kind = lane & 3;
+  const int pj = __shfl_sync(0xffffffffu, page, j & (kPagesPerTile - 1));
+  if (lane < 4 * kPagesPerTile && pj >= 0) {
+    const size_t blk = (size_t)pj * p.num_kv_heads + s.h;
+    if (kind == 0)
+      bulk_g2s(smem_u32(stage) + j * kBlock, p.k_pages + blk * kBlock, kBlock, ring_bar);
+    else if (kind == 1)
+      bulk_g2s(smem_u32(stage) + C::kRingCodes + j * kBlock, p.v_pages + blk * kBlock, kBlock,
+               ring_bar);
+    else if (kind == 2)
+      bulk_g2s(smem_u32(scales) + j * kScaleBlock, p.k_scales + blk * kPageSize, kScaleBlock,
+               scale_bar);
+    else
+      bulk_g2s(smem_u32(scales) + kTileKeys * 4 + j * kScaleBlock, p.v_scales + blk * kPageSize,
+               kScaleBlock, scale_bar);
   }
 }
 
@@ -308,14 +337,20 @@ __device__ __forceinline__ void stage_tile(const AttnParams& p, const Seg& s, in
 template <int D>
 __device__ __forceinline__ void convert_codes(const uint8_t* src, uint8_t* dst, int lt) {
   constexpr int kUnits = kTileKeys * D / 8;
+  constexpr int kPer = kUnits / kLoadThreads;
+  uint2 w[kPer];
 #pragma unroll
-  for (int q = 0; q < kUnits / kLoadThreads; ++q) {
+  for (int q = 0; q < kPer; ++q) {
+    const int u = q * kLoadThreads + lt;
+    w[q] = *reinterpret_cast<const uint2*>(src + (u / (D / 8)) * D + (u % (D / 8)) * 8);
+  }
+#pragma unroll
+  for (int q = 0; q < kPer; ++q) {
     const int u = q * kLoadThreads + lt;
     const int n = u / (D / 8), c8 = u % (D / 8);
-    const uint2 w = *reinterpret_cast<const uint2*>(src + n * D + c8 * 8);
     uint4 h;
-    i8x4_to_h2x2(w.x, h.x, h.y);
-    i8x4_to_h2x2(w.y, h.z, h.w);
+    i8x4_to_h2x2(w[q].x, h.x, h.y);
+    i8x4_to_h2x2(w[q].y, h.z, h.w);
     const uint32_t a = (c8 / 8) * (kTileKeys * 128) + n * 128 + (((c8 & 7) ^ (n & 7)) << 4);
     *reinterpret_cast<uint4*>(dst + a) = h;
   }
@@ -325,19 +360,27 @@ __device__ __forceinline__ void convert_codes(const uint8_t* src, uint8_t* dst, 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
   using C = Cfg<D>;
+  static_assert(sizeof(Smem) <= C::kBarBytes, "barrier area");
   extern __shared__ uint8_t smem_raw[];
+  const PlanHeader* hd = reinterpret_cast<const PlanHeader*>(p.ws);
+  const int total = hd->total_tiles[kClassTensor];
+  const int ncta = hd->ncta[kClassTensor];
+  if ((int)blockIdx.x >= ncta) return;
+  // 128-byte swizzled operand tiles need a 1024-byte aligned base
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  uint8_t* kbuf = smem;                                   // [kStages] fp16 K tiles
-  uint8_t* vbuf = smem + kStages * C::kTileBytes;         // [kStages] fp16 V tiles
-  float* kscale = reinterpret_cast<float*>(smem + C::kSmemTiles);   // [kStages][64]
-  float* vscale = kscale + kStages * kTileKeys;                     // [kStages][64]
-  uint8_t* ring = smem + C::kSmemTiles + C::kSmemScales;            // [kRing][stage]
-  Smem* sh = reinterpret_cast<Smem*>(ring + C::kSmemRing);
+  if (smem - smem_raw + C::kSmemUsed > C::kSmemBytes) {
+    if (threadIdx.x == 0) report(p.device_status, SPLASH_DEVICE_INTERNAL);
+    return;
+  }
+  uint8_t* kbuf = smem + C::kOffK;
+  uint8_t* vbuf = smem + C::kOffV;
+  uint8_t* ring = smem + C::kOffRing;
+  float* scales = reinterpret_cast<float*>(smem + C::kOffScales);   // [3][K 64, V 64]
+  Smem* sh = reinterpret_cast<Smem*>(smem + C::kOffBars);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int B = p.num_seqs, Hkv = p.num_kv_heads, G = p.group;
-  const PlanHeader* hd = reinterpret_cast<const PlanHeader*>(p.ws);
   const WorkspaceLayout L = make_layout(B, Hkv, D, hd->rows_bound);
   const int* q_off = reinterpret_cast<const int*>(p.ws + L.q_off);
   const int* seq_T = reinterpret_cast<const int*>(p.ws + L.seq_T);
@@ -349,10 +392,6 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
   float* o_part = reinterpret_cast<float*>(p.ws + L.o_part);
   float* lse_part = reinterpret_cast<float*>(p.ws + L.lse_part);
 
-  const int total = hd->total_tiles[kClassTensor];
-  const int ncta = hd->ncta[kClassTensor];
-  if ((int)blockIdx.x >= ncta) return;
-
   if (tid == 0) {
     for (int s = 0; s < kRing; ++s) {
       mbar_init(smem_u32(&sh->ring_full[s]), 1);
@@ -360,12 +399,15 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
     }
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&sh->kv_full[s]), kLoadThreads);
-      mbar_init(smem_u32(&sh->v_free[s]), 1);
       mbar_init(smem_u32(&sh->k_free[s]), 1);
       mbar_init(smem_u32(&sh->s_full[s]), 1);
       mbar_init(smem_u32(&sh->p_full[s]), 32 * kSoftmaxWarps);
+      mbar_init(smem_u32(&sh->p_free[s]), 1);
     }
-    mbar_init(smem_u32(&sh->o_done), 1);
+    for (int s = 0; s < kVStages; ++s) {
+      mbar_init(smem_u32(&sh->sc_full[s]), 1);
+      mbar_init(smem_u32(&sh->v_free[s]), 1);
+    }
     mbar_init(smem_u32(&sh->q_full), 32 * kSoftmaxWarps);
     mbar_init(smem_u32(&sh->drain), 1);
     sh->abort_flag = 0;
@@ -389,7 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
     // ===================================================== softmax + epilogue
     const int r = tid;                                    // query row = TMEM lane
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    int g = 0, nsegs = 0;
+    int g = 0;
     Seg s;
     bool ok = true;
     while (ok && iter.next(s)) {
@@ -417,7 +459,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
         // 2^e with max|q| * 2^e in [2^14, 2^15)
         int e = 0;
         if (amax > 0.f) e = 14 - (int)((__float_as_uint(amax) >> 23) & 0xff) + 127;
-        if (amax > 0.f && ((__float_as_uint(amax) >> 23) & 0xff) == 0) e = 14 + 126;  // subnormal max
+        if (amax > 0.f && ((__float_as_uint(amax) >> 23) & 0xff) == 0) e = 14 + 126;
         e = max(-126, min(127, e));
         const float up = __uint_as_float((uint32_t)(e + 127) << 23);
         rowfac = p.sm_scale_log2 / up;
@@ -445,22 +487,25 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
 
       float m = -INFINITY, l = 0.f;
       for (int it = s.i0; it < s.i1 && ok; ++it, ++g) {
-        const int st = g % kStages;
-        const uint32_t ph = (g / kStages) & 1;
-        ok = sync.wait(smem_u32(&sh->kv_full[st]), ph) && sync.wait(smem_u32(&sh->s_full[st]), ph);
+        const int st = g % kStages, vst = g % kVStages;
+        ok = sync.wait(smem_u32(&sh->sc_full[vst]), (g / kVStages) & 1) &&
+             sync.wait(smem_u32(&sh->s_full[st]), (g / kStages) & 1);
         if (!ok) break;
         fence_after();
         uint32_t pw[32];
         float alpha = 1.f;
         if (warp_live) {
           const int k0 = it * kTileKeys;
-          const float4* ks4 = reinterpret_cast<const float4*>(kscale + st * kTileKeys);
-          const float4* vs4 = reinterpret_cast<const float4*>(vscale + st * kTileKeys);
+          const float4* ks4 = reinterpret_cast<const float4*>(scales + vst * 2 * kTileKeys);
+          const float4* vs4 = ks4 + kTileKeys / 4;
           uint32_t s0[32], s1[32];
           tmem_ld32(tmem + lane_base + C::kSCol + st * kTileKeys, s0);
           tmem_ld32(tmem + lane_base + C::kSCol + st * kTileKeys + 32, s1);
           tmem_wait_ld();
-          // x = S * sK (packed fp32x2), masked columns -> -inf
+          const int nvis = row_live ? min(kTileKeys, lim - k0 + 1) : 0;   // visible keys
+          const bool full = nvis == kTileKeys;
+          // x = S * sK (packed fp32x2); masked columns -> -inf (their scales
+          // are not read: pages past the end may hold anything)
           float2 x[32];
 #pragma unroll
           for (int j4 = 0; j4 < 16; ++j4) {
@@ -471,8 +516,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
             x[2 * j4 + 1] = __fmul2_rn(make_float2(__uint_as_float(src[2]), __uint_as_float(src[3])),
                                        make_float2(kq.z, kq.w));
           }
-          const int nvis = row_live ? min(kTileKeys, lim - k0 + 1) : 0;   // visible keys in tile
-          if (nvis < kTileKeys) {
+          if (!full) {
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
               if (2 * j >= nvis) x[j].x = -INFINITY;
@@ -496,7 +540,14 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
           float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
           for (int j4 = 0; j4 < 16; ++j4) {
-            const float4 vq = vs4[j4];
+            float4 vq = vs4[j4];
+            if (!full) {      // scales of masked keys are not trusted
+              const int j = 4 * j4;
+              if (j >= nvis) vq.x = 0.f;
+              if (j + 1 >= nvis) vq.y = 0.f;
+              if (j + 2 >= nvis) vq.z = 0.f;
+              if (j + 3 >= nvis) vq.w = 0.f;
+            }
             const float2 e0 = __ffma2_rn(x[2 * j4], rf2, nb2);
             const float2 e1 = __ffma2_rn(x[2 * j4 + 1], rf2, nb2);
             const float2 p0 = make_float2(ex2(e0.x), ex2(e0.y));
@@ -511,9 +562,11 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
           l = l * alpha + (acc.x + acc.y);
         }
         // a rescale of O waits for the previous tile's PV (rare: the running
-        // max is only moved when it grows by more than 2^8)
+        // max is only moved when it grows by more than 2^8). p_free of that
+        // tile's buffer: its previous phase (PV three tiles back) is complete,
+        // so a parity wait cannot be satisfied by an older phase.
         if (it > s.i0 && warp_live && __any_sync(0xffffffffu, alpha != 1.f)) {
-          ok = sync.wait(smem_u32(&sh->o_done), (g - 1) & 1);
+          ok = sync.wait(smem_u32(&sh->p_free[(g - 1) % kStages]), ((g - 1) / kStages) & 1);
           if (!ok) break;
           fence_after();
 #pragma unroll 1
@@ -535,7 +588,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
       }
       if (!ok) break;
       // epilogue: last PV of the segment complete -> normalise, write out
-      ok = sync.wait(smem_u32(&sh->o_done), (g - 1) & 1);
+      ok = sync.wait(smem_u32(&sh->p_free[(g - 1) % kStages]), ((g - 1) / kStages) & 1);
       if (!ok) break;
       fence_after();
       if (warp_live) {
@@ -582,7 +635,6 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
         }
       }
       fence_before();
-      ++nsegs;
     }
   } else if (warp < kSoftmaxWarps + kLoadWarps) {
     // =========================================================== converters
@@ -592,52 +644,52 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
     bool ok = true;
     while (ok && iter.next(s)) {
       for (int it = s.i0; it < s.i1; ++it, ++g) {
-        const int r = g % kRing, st = g % kStages;
+        const int r = g % kRing, st = g % kStages, vst = g % kVStages;
         ok = sync.wait(smem_u32(&sh->ring_full[r]), (g / kRing) & 1);
         if (!ok) break;
         const uint8_t* stage = ring + r * C::kRingStage;
-        const uint32_t free_par = ((g / kStages) & 1) ^ 1;
-        ok = sync.wait(smem_u32(&sh->k_free[st]), free_par);
+        ok = sync.wait(smem_u32(&sh->k_free[st]), ((g / kStages) & 1) ^ 1);
         if (!ok) break;
         convert_codes<D>(stage, kbuf + st * C::kTileBytes, lt);
-        ok = sync.wait(smem_u32(&sh->v_free[st]), free_par);
+        ok = sync.wait(smem_u32(&sh->v_free[vst]), ((g / kVStages) & 1) ^ 1);
         if (!ok) break;
-        convert_codes<D>(stage + C::kRingCodes, vbuf + st * C::kTileBytes, lt);
-        if (lt < 2 * kTileKeys) {
-          const int n = lt % kTileKeys;
-          const int key = it * kTileKeys + n;
-          const bool valid = key < s.Lk && ((sh->ring_valid[r] >> (n / kPageSize)) & 1);
-          const float* src = reinterpret_cast<const float*>(stage + 2 * C::kRingCodes);
-          if (lt < kTileKeys) kscale[st * kTileKeys + n] = valid ? src[n] : 0.f;
-          else vscale[st * kTileKeys + n] = valid ? src[kTileKeys + n] : 0.f;
-        }
+        convert_codes<D>(stage + C::kRingCodes, vbuf + vst * C::kTileBytes, lt);
+        mbar_arrive(smem_u32(&sh->ring_empty[r]));
         fence_async_smem();
         mbar_arrive(smem_u32(&sh->kv_full[st]));
-        mbar_arrive(smem_u32(&sh->ring_empty[r]));
       }
     }
   } else if (warp == kProducerWarp) {
     // ============================================================ producer
-    if (lane == 0) {
-      int g = 0;
-      Seg s;
-      bool ok = true;
-      while (ok && iter.next(s)) {
-        for (int it = s.i0; it < s.i1; ++it, ++g) {
-          const int r = g % kRing;
-          ok = sync.wait(smem_u32(&sh->ring_empty[r]), ((g / kRing) & 1) ^ 1);
-          if (!ok) break;
-          stage_tile<D>(p, s, it, ring + r * C::kRingStage, smem_u32(&sh->ring_full[r]),
-                        &sh->ring_valid[r]);
+    int g = 0;
+    Seg s;
+    bool ok = true;
+    while (ok && iter.next(s)) {
+      for (int it = s.i0; it < s.i1; ++it, ++g) {
+        const int r = g % kRing, vst = g % kVStages;
+        if (lane == 0) {
+          // ring stage free (converted), scale stage free (PV three tiles back done)
+          ok = sync.wait(smem_u32(&sh->ring_empty[r]), ((g / kRing) & 1) ^ 1) &&
+               sync.wait(smem_u32(&sh->v_free[vst]), ((g / kVStages) & 1) ^ 1);
         }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        stage_tile<D>(p, s, it, ring + r * C::kRingStage, scales + vst * 2 * kTileKeys,
+                      smem_u32(&sh->ring_full[r]), smem_u32(&sh->sc_full[vst]), lane);
       }
     }
-    __syncwarp();
   } else {
     // ================================================================= MMA
     if (lane == 0) {
       constexpr uint32_t kIdescQK = idesc_f16(128, kTileKeys, 0);
       constexpr uint32_t kIdescPV = idesc_f16(128, D, 1);
+      // descriptors of k-step 0 of every buffer; k-steps add byte offsets >> 4
+      uint64_t kdesc[kStages], vdesc[kVStages];
+#pragma unroll
+      for (int i = 0; i < kStages; ++i) kdesc[i] = sdesc(smem_u32(kbuf + i * C::kTileBytes), 16, 1024);
+#pragma unroll
+      for (int i = 0; i < kVStages; ++i)
+        vdesc[i] = sdesc(smem_u32(vbuf + i * C::kTileBytes), kTileKeys * 128, 1024);
       int g = 0, nsegs = 0;
       Seg s;
       bool ok = true;
@@ -646,45 +698,43 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
         if (!ok) break;
         fence_after();
         const int n = s.i1 - s.i0;
-        // QK(i) and PV(i) are issued in their own orders, each as soon as its
-        // inputs are ready; QK(i) also needs PV(i-2) issued (S/P buffer reuse;
-        // MMAs run in issue order). In-flight limit: bounded by the same timeout.
+        // PV(i) and QK(i) are issued in their own orders, each as soon as its
+        // inputs are ready (PV first: it frees V buffers). QK(i) overwrites the
+        // S/P buffer that PV(i-2) reads as its A operand: issue order does not
+        // order that write after the read, so QK(i) waits for PV(i-2) to
+        // complete (p_free).
         int nq = 0, np = 0;
         unsigned long long t_idle = 0;
         while (np < n) {
           bool progressed = false;
-          if (nq < n && nq <= np + 1) {
-            const int gi = g + nq, st = gi % kStages;
-            if (mbar_try_wait(smem_u32(&sh->kv_full[st]), (gi / kStages) & 1)) {
+          if (np < nq) {
+            const int gi = g + np, st = gi % kStages, vst = gi % kVStages;
+            if (mbar_test_wait(smem_u32(&sh->p_full[st]), (gi / kStages) & 1)) {
               fence_after();
-              const uint32_t kaddr = smem_u32(kbuf + st * C::kTileBytes);
 #pragma unroll
-              for (int kk = 0; kk < D / 16; ++kk) {
-                const uint64_t bd =
-                    sdesc(kaddr + (kk / 4) * (kTileKeys * 128) + (kk % 4) * 32, 16, 1024);
-                mma_ts(tmem + C::kSCol + st * kTileKeys, tmem + C::kQCol + kk * 8, bd,
-                       kIdescQK, kk > 0);
-              }
-              mma_commit(smem_u32(&sh->s_full[st]));
-              mma_commit(smem_u32(&sh->k_free[st]));
-              ++nq;
+              for (int kk = 0; kk < kTileKeys / 16; ++kk)
+                mma_ts(tmem + C::kOCol, tmem + C::kSCol + st * kTileKeys + kk * 8,
+                       vdesc[vst] + (uint64_t)((kk * 16 * 128) >> 4), kIdescPV,
+                       (np == 0 && kk == 0) ? 0u : 1u);
+              mma_commit(smem_u32(&sh->v_free[vst]));
+              mma_commit(smem_u32(&sh->p_free[st]));
+              ++np;
               progressed = true;
             }
           }
-          if (np < nq) {
-            const int gi = g + np, st = gi % kStages;
-            if (mbar_try_wait(smem_u32(&sh->p_full[st]), (gi / kStages) & 1)) {
+          if (nq < n && nq <= np + 1) {
+            const int gi = g + nq, st = gi % kStages;
+            if (mbar_test_wait(smem_u32(&sh->p_free[st]), ((gi / kStages) & 1) ^ 1) &&
+                mbar_test_wait(smem_u32(&sh->kv_full[st]), (gi / kStages) & 1)) {
               fence_after();
-              const uint32_t vaddr = smem_u32(vbuf + st * C::kTileBytes);
 #pragma unroll
-              for (int kk = 0; kk < kTileKeys / 16; ++kk) {
-                const uint64_t bd = sdesc(vaddr + kk * 16 * 128, kTileKeys * 128, 1024);
-                mma_ts(tmem + C::kOCol, tmem + C::kSCol + st * kTileKeys + kk * 8, bd,
-                       kIdescPV, (np == 0 && kk == 0) ? 0u : 1u);
-              }
-              mma_commit(smem_u32(&sh->v_free[st]));
-              mma_commit(smem_u32(&sh->o_done));
-              ++np;
+              for (int kk = 0; kk < D / 16; ++kk)
+                mma_ts(tmem + C::kSCol + st * kTileKeys, tmem + C::kQCol + kk * 8,
+                       kdesc[st] + (uint64_t)(((kk / 4) * (kTileKeys * 128) + (kk % 4) * 32) >> 4),
+                       kIdescQK, kk > 0);
+              mma_commit(smem_u32(&sh->s_full[st]));
+              mma_commit(smem_u32(&sh->k_free[st]));
+              ++nq;
               progressed = true;
             }
           }
