@@ -16,8 +16,10 @@
 // folded into P before P is rounded to fp16.
 //
 // Warp roles (448 threads):
-//   warps 0-3   softmax + epilogue: thread = TMEM lane = query row
-//   warps 4-11  converters: int8 codes from the staging ring -> fp16 in
+//   warps 0-7   softmax + epilogue: warp w owns TMEM lanes (rows) 32(w%4) +
+//               16(w/4) .. +15; with the 16x256b load shape each row is spread
+//               over 4 threads (2 rows per thread, row reductions = 2 shuffles)
+//   warps 8-11  converters: int8 codes from the staging ring -> fp16 in
 //               registers -> 128B-swizzled SMEM tiles (K: K-major, V: MN-major)
 //   warp  12    TMEM allocation and the single MMA-issuing thread
 //   warp  13    producer: bulk async copies (TMA, untiled) of whole
@@ -38,8 +40,8 @@ constexpr int kPagesPerTile = kTileKeys / kPageSize;
 constexpr int kStages = 2;                    // S/P buffers in TMEM, fp16 K tiles
 constexpr int kVStages = 3;                   // fp16 V tiles and the scale arrays
 constexpr int kRing = 2;                      // int8 staging stages
-constexpr int kSoftmaxWarps = 4;
-constexpr int kLoadWarps = 8;
+constexpr int kSoftmaxWarps = 8;              // 2 per TMEM lane quarter, 16 rows each
+constexpr int kLoadWarps = 4;
 constexpr int kLoadThreads = 32 * kLoadWarps;
 constexpr int kMmaWarp = kSoftmaxWarps + kLoadWarps;
 constexpr int kProducerWarp = kMmaWarp + 1;
@@ -205,6 +207,35 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32
       ::"r"(taddr), SPLASH_W8(0), SPLASH_W8(8), SPLASH_W8(16), SPLASH_W8(24)
       : "memory");
 }
+// 16 lanes x 64 columns (16x256b, 8 repetitions): thread t holds, for
+// repetition i, columns 8i + 2(t%4) + {0,1} of lane base + t/4 (v[4i], v[4i+1])
+// and of lane base + 8 + t/4 (v[4i+2], v[4i+3])
+__device__ __forceinline__ void tmem_ld16x256_x8(uint32_t taddr, uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+      "%28, %29, %30, %31}, [%32];"
+      : SPLASH_R8(0), SPLASH_R8(8), SPLASH_R8(16), SPLASH_R8(24)
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st16x256_x8(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.16x256b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+      "%28, %29, %30, %31, %32};"
+      ::"r"(taddr), SPLASH_W8(0), SPLASH_W8(8), SPLASH_W8(16), SPLASH_W8(24)
+      : "memory");
+}
+// 16 lanes x 32 columns (16x128b, 16 repetitions): repetition i holds column
+// 4i + t%4 of lane base + t/4 (v[2i]) and of lane base + 8 + t/4 (v[2i+1])
+__device__ __forceinline__ void tmem_st16x128_x16(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.16x128b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+      "%28, %29, %30, %31, %32};"
+      ::"r"(taddr), SPLASH_W8(0), SPLASH_W8(8), SPLASH_W8(16), SPLASH_W8(24)
+      : "memory");
+}
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -283,57 +314,101 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
       : "memory");
 }
 
-// Producer (one warp): stage tile `it` of segment s. Lanes 0..3 look up the
-// tile's page ids in parallel; lanes 0..15 issue one bulk copy each (page
-// j = lane/4: K codes, V codes into the ring stage; K scales, V scales into the
-// scale arrays). Pages past the sequence end or with an invalid id are
+// Page ids of a sequence, 32 at a time: lane l holds entry base + l of the
+// sequence's page-table row (-1 past the pages the sequence needs). The next
+// window is fetched when the current one is first used, so the table read
+// latency is paid once per 8 tiles and mostly hidden.
+struct PageWindow {
+  int b = -1, base = 0, cur = -1;
+  int nb = -1, nbase = 0, nxt = -1;
+  __device__ __forceinline__ static int fetch(const AttnParams& p, int b, int base, int npages,
+                                              int lane) {
+    const int i = base + lane;
+    return i < npages ? p.page_table[(size_t)b * p.max_pages_per_seq + i] : -1;
+  }
+  // make entries [first, first + 4) of sequence b available; returns the id of
+  // page `first + (lane & 3)` in every lane
+  __device__ __forceinline__ int get(const AttnParams& p, int sb, int first, int npages,
+                                     int lane) {
+    const int want = first & ~31;
+    if (sb != b || want != base) {
+      if (sb == nb && want == nbase) {
+        cur = nxt;
+      } else {
+        cur = fetch(p, sb, want, npages, lane);
+      }
+      b = sb;
+      base = want;
+      nb = sb;
+      nbase = want + 32;
+      nxt = fetch(p, sb, nbase, npages, lane);      // prefetch the next window
+    }
+    return __shfl_sync(0xffffffffu, cur, (first - base) + (lane & 3));
+  }
+};
+
+// Producer (one warp): stage tile `it` of segment s. The tile's 4 page ids
+// come from the page window; lanes 0..7 issue one bulk copy each (K or V codes
+// of one page into the ring stage); every lane moves 16 bytes of scales into
+// the scale arrays with cp.async. Pages past the sequence end or with an invalid id are
 // skipped: their stale codes are finite and the softmax gives their keys
 // probability 0 without reading their scales.
 template <int D>
 __device__ __forceinline__ void stage_tile(const AttnParams& p, const Seg& s, int it,
                                            uint8_t* stage, float* scales, uint32_t ring_bar,
-                                           uint32_t scale_bar, int lane) {
+                                           uint32_t scale_bar, int lane, PageWindow& win) {
   using C = Cfg<D>;
   const int k0 = it * kTileKeys;
-  const int32_t* ptab = p.page_table + (size_t)s.b * p.max_pages_per_seq;
-  int page = -1;
-  if (lane < kPagesPerTile && k0 + kPageSize * lane < s.Lk) {
-    page = ptab[(k0 / kPageSize) + lane];
-    if (page < 0 || page >= p.num_pages) {
-      report(p.device_status, SPLASH_DEVICE_BAD_PAGE);
-      page = -1;
+  const int npages = (s.Lk + kPageSize - 1) / kPageSize;
+  // every lane holds the id of page (lane & 3) of this tile
+  int page = win.get(p, s.b, k0 / kPageSize, npages, lane);
+  const int j = lane & 3;
+  if (k0 + kPageSize * j >= s.Lk) page = -1;
+  if (page >= p.num_pages) page = -1;
+  const bool bad = (k0 + kPageSize * j < s.Lk) && page < 0;
+  if (bad && lane < kPagesPerTile) report(p.device_status, SPLASH_DEVICE_BAD_PAGE);
+  const int mask = (int)(__ballot_sync(0xffffffffu, page >= 0 && lane < kPagesPerTile) &
+                         ((1u << kPagesPerTile) - 1));
+  constexpr uint32_t kBlock = kPageSize * D;          // codes of one (page, head)
+  if (lane == 0) mbar_expect_tx(ring_bar, (uint32_t)__popc(mask) * (2 * kBlock));
+  __syncwarp();
+  // codes: one bulk copy per (page, tensor), lanes 0..7
+  if (lane < 2 * kPagesPerTile) {
+    const int pj = __shfl_sync(0x000000ffu, page, lane >> 1);
+    if (pj >= 0) {
+      const size_t blk = (size_t)pj * p.num_kv_heads + s.h;
+      const int jj = lane >> 1;
+      if ((lane & 1) == 0)
+        bulk_g2s(smem_u32(stage) + jj * kBlock, p.k_pages + blk * kBlock, kBlock, ring_bar);
+      else
+        bulk_g2s(smem_u32(stage) + C::kRingCodes + jj * kBlock, p.v_pages + blk * kBlock,
+                 kBlock, ring_bar);
     }
   }
-  const int mask = (int)(__ballot_sync(0xffffffffu, page >= 0) & ((1u << kPagesPerTile) - 1));
-  constexpr uint32_t kBlock = kPageSize * D;          // codes of one (page, head)
-  constexpr uint32_t kScaleBlock = kPageSize * 4;
-  if (lane == 0) {
-    mbar_expect_tx(ring_bar, (uint32_t)__popc(mask) * (2 * kBlock));
-    mbar_expect_tx(scale_bar, (uint32_t)__popc(mask) * (2 * kScaleBlock));
+  // scales: 16 bytes per lane by cp.async (lanes 0..15 K, 16..31 V; page
+  // (lane & 15) / 4, slots 4 * (lane & 3) ..); each lane's arrival on the
+  // scale barrier fires when its copy has landed
+  const int sj = (lane & 15) >> 2;
+  const int ps = __shfl_sync(0xffffffffu, page, sj);
+  if (ps >= 0) {
+    const float* src = (lane < 16 ? p.k_scales : p.v_scales) +
+                       ((size_t)ps * p.num_kv_heads + s.h) * kPageSize + 4 * (lane & 3);
+    const uint32_t dst = smem_u32(scales) + (lane < 16 ? 0 : kTileKeys * 4) +
+                         (sj * kPageSize + 4 * (lane & 3)) * 4;
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
   }
-  __syncwarp();
-  const int j = lane >> 2, kind = lane & 3;
-  const int pj = __shfl_sync(0xffffffffu, page, j & (kPagesPerTile - 1));
-  if (lane < 4 * kPagesPerTile && pj >= 0) {
-    const size_t blk = (size_t)pj * p.num_kv_heads + s.h;
-    if (kind == 0)
-      bulk_g2s(smem_u32(stage) + j * kBlock, p.k_pages + blk * kBlock, kBlock, ring_bar);
-    else if (kind == 1)
-      bulk_g2s(smem_u32(stage) + C::kRingCodes + j * kBlock, p.v_pages + blk * kBlock, kBlock,
-               ring_bar);
-    else if (kind == 2)
-      bulk_g2s(smem_u32(scales) + j * kScaleBlock, p.k_scales + blk * kPageSize, kScaleBlock,
-               scale_bar);
-    else
-      bulk_g2s(smem_u32(scales) + kTileKeys * 4 + j * kScaleBlock, p.v_scales + blk * kPageSize,
-               kScaleBlock, scale_bar);
-  }
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(scale_bar)
+               : "memory");
 }
 
-// Converters: 8 consecutive codes (one key, channels d0..d0+7) per unit; the
-// 8 threads of a quarter warp cover one 128-byte swizzled row, so the 16-byte
-// stores are free of bank conflicts. fp16 element (key n, d) lives at block
-// d/64, row n, 16-byte chunk ((d%64)/8) ^ (n%8) (SWIZZLE_128B, 1024-byte atoms).
+// Tile row of key n: keys are permuted inside a tile (K and V alike, so the
+// contraction over keys is unchanged) so that S/P column 8i + 2q + b, which the
+// 16x256b TMEM load hands to the thread with q = lane % 4, holds key
+// 16q + 2i + b: each softmax thread then owns 16 consecutive keys.
+__host__ __device__ constexpr int tile_row_of_key(int n) {
+  return 8 * ((n % 16) / 2) + 2 * (n / 16) + (n % 2);
+}
+
 template <int D>
 __device__ __forceinline__ void convert_codes(const uint8_t* src, uint8_t* dst, int lt) {
   constexpr int kUnits = kTileKeys * D / 8;
@@ -347,7 +422,7 @@ __device__ __forceinline__ void convert_codes(const uint8_t* src, uint8_t* dst, 
 #pragma unroll
   for (int q = 0; q < kPer; ++q) {
     const int u = q * kLoadThreads + lt;
-    const int n = u / (D / 8), c8 = u % (D / 8);
+    const int n = tile_row_of_key(u / (D / 8)), c8 = u % (D / 8);
     uint4 h;
     i8x4_to_h2x2(w[q].x, h.x, h.y);
     i8x4_to_h2x2(w[q].y, h.z, h.w);
@@ -405,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
       mbar_init(smem_u32(&sh->p_free[s]), 1);
     }
     for (int s = 0; s < kVStages; ++s) {
-      mbar_init(smem_u32(&sh->sc_full[s]), 1);
+      mbar_init(smem_u32(&sh->sc_full[s]), 32);     // one cp.async arrival per producer lane
       mbar_init(smem_u32(&sh->v_free[s]), 1);
     }
     mbar_init(smem_u32(&sh->q_full), 32 * kSoftmaxWarps);
@@ -429,63 +504,79 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
 
   if (warp < kSoftmaxWarps) {
     // ===================================================== softmax + epilogue
-    const int r = tid;                                    // query row = TMEM lane
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const int lb = 32 * (warp % 4) + 16 * (warp / 4);     // first TMEM lane (row) of the warp
+    const uint32_t lane_base = (uint32_t)lb << 16;
+    const int quad = lane & 3;                            // column pair within 8 columns
+    const int rr[2] = {lb + (lane >> 2), lb + 8 + (lane >> 2)};
     int g = 0;
     Seg s;
     bool ok = true;
     while (ok && iter.next(s)) {
-      const bool warp_live = warp * 32 < s.R;
-      const bool row_live = r < s.R;
-      const int tt = r / G, gg = r % G;
-      const int lim = s.ctx + tt;                         // last visible key
-      float rowfac = 0.f;
-      // Q row -> TMEM (fp16 after an exact power-of-two rescale)
+      const bool warp_live = lb < s.R;
+      bool live[2];
+      int lim[2];
+      size_t qrow_off[2];
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        live[k] = rr[k] < s.R;
+        const int tt = rr[k] / G, gg = rr[k] % G;
+        lim[k] = s.ctx + tt;                              // last visible key of the row
+        qrow_off[k] = (size_t)(q_off[s.b] + tt) * p.num_q_heads + s.h * G + gg;
+      }
+      float rowfac[2] = {0.f, 0.f};
+      // Q rows -> TMEM as fp16 after an exact per-row power-of-two rescale.
+      // Thread covers d = 8i + 2*quad + {0,1} (i < D/8) of both rows.
       if (warp_live) {
-        const __nv_bfloat16* qrow =
-            p.q + ((size_t)(q_off[s.b] + tt) * p.num_q_heads + s.h * G + gg) * D;
-        float amax = 0.f;
-        if (row_live) {
-          for (int d = 0; d < D; d += 8) {
-            const uint4 w = *reinterpret_cast<const uint4*>(qrow + d);
-            const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&w);
+        float up[2];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 f = __bfloat1622float2(h2[e]);
-              amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+        for (int k = 0; k < 2; ++k) {
+          float amax = 0.f;
+          if (live[k]) {
+            const __nv_bfloat162* qr =
+                reinterpret_cast<const __nv_bfloat162*>(p.q + qrow_off[k] * D) + quad;
+#pragma unroll 8
+            for (int i = 0; i < D / 8; ++i) {
+              const float2 f = __bfloat1622float2(qr[4 * i]);
+              amax = fmax3(amax, fabsf(f.x), fabsf(f.y));
             }
           }
+          amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+          amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+          // 2^e with max|q| * 2^e in [2^14, 2^15)
+          int e = 0;
+          const int ex = (int)((__float_as_uint(amax) >> 23) & 0xff);
+          if (amax > 0.f) e = ex == 0 ? 14 + 126 : 14 - ex + 127;
+          e = max(-126, min(127, e));
+          up[k] = __uint_as_float((uint32_t)(e + 127) << 23);
+          rowfac[k] = p.sm_scale_log2 / up[k];
         }
-        // 2^e with max|q| * 2^e in [2^14, 2^15)
-        int e = 0;
-        if (amax > 0.f) e = 14 - (int)((__float_as_uint(amax) >> 23) & 0xff) + 127;
-        if (amax > 0.f && ((__float_as_uint(amax) >> 23) & 0xff) == 0) e = 14 + 126;
-        e = max(-126, min(127, e));
-        const float up = __uint_as_float((uint32_t)(e + 127) << 23);
-        rowfac = p.sm_scale_log2 / up;
 #pragma unroll 1
-        for (int c0 = 0; c0 < D; c0 += 64) {
-          uint32_t v[32];
+        for (int c0 = 0; c0 < D / 2; c0 += 64) {          // 64 packed columns per pass
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            uint4 w = make_uint4(0, 0, 0, 0);
-            if (row_live) w = *reinterpret_cast<const uint4*>(qrow + c0 + 8 * k);
-            const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&w);
+          for (int half = 0; half < 2; ++half) {
+            uint32_t v[32];
 #pragma unroll
-            for (int e2 = 0; e2 < 4; ++e2) {
-              const float2 f = __bfloat1622float2(h2[e2]);
-              __half2 hv = __floats2half2_rn(f.x * up, f.y * up);
-              v[4 * k + e2] = *reinterpret_cast<uint32_t*>(&hv);
+            for (int i = 0; i < 16; ++i) {
+              const int col = c0 + 32 * half + 4 * i + quad;     // packed column = d pair
+#pragma unroll
+              for (int k = 0; k < 2; ++k) {
+                float2 f = make_float2(0.f, 0.f);
+                if (live[k])
+                  f = __bfloat1622float2(
+                      reinterpret_cast<const __nv_bfloat162*>(p.q + qrow_off[k] * D)[col]);
+                __half2 hv = __floats2half2_rn(f.x * up[k], f.y * up[k]);
+                v[2 * i + k] = *reinterpret_cast<uint32_t*>(&hv);
+              }
             }
+            tmem_st16x128_x16(tmem + lane_base + C::kQCol + c0 + 32 * half, v);
           }
-          tmem_st32(tmem + lane_base + C::kQCol + c0 / 2, v);
         }
         tmem_wait_st();
       }
       fence_before();
       mbar_arrive(smem_u32(&sh->q_full));
 
-      float m = -INFINITY, l = 0.f;
+      float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};   // l: this thread's columns
       for (int it = s.i0; it < s.i1 && ok; ++it, ++g) {
         const int st = g % kStages, vst = g % kVStages;
         ok = sync.wait(smem_u32(&sh->sc_full[vst]), (g / kVStages) & 1) &&
@@ -493,94 +584,123 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
         if (!ok) break;
         fence_after();
         uint32_t pw[32];
-        float alpha = 1.f;
+        float alpha[2] = {1.f, 1.f};
         if (warp_live) {
           const int k0 = it * kTileKeys;
-          const float4* ks4 = reinterpret_cast<const float4*>(scales + vst * 2 * kTileKeys);
-          const float4* vs4 = ks4 + kTileKeys / 4;
-          uint32_t s0[32], s1[32];
-          tmem_ld32(tmem + lane_base + C::kSCol + st * kTileKeys, s0);
-          tmem_ld32(tmem + lane_base + C::kSCol + st * kTileKeys + 32, s1);
+          const float* ks = scales + vst * 2 * kTileKeys;
+          const float* vs = ks + kTileKeys;
+          uint32_t sv[32];
+          tmem_ld16x256_x8(tmem + lane_base + C::kSCol + st * kTileKeys, sv);
           tmem_wait_ld();
-          const int nvis = row_live ? min(kTileKeys, lim - k0 + 1) : 0;   // visible keys
-          const bool full = nvis == kTileKeys;
           // x = S * sK (packed fp32x2); masked columns -> -inf (their scales
           // are not read: pages past the end may hold anything)
-          float2 x[32];
+          // this thread's keys: 16*quad + 2i + {0,1} (see tile_row_of_key)
+          float2 ks2[8], x[2][8];
 #pragma unroll
-          for (int j4 = 0; j4 < 16; ++j4) {
-            const float4 kq = ks4[j4];
-            const uint32_t* src = j4 < 8 ? &s0[4 * j4] : &s1[4 * j4 - 32];
-            x[2 * j4] = __fmul2_rn(make_float2(__uint_as_float(src[0]), __uint_as_float(src[1])),
-                                   make_float2(kq.x, kq.y));
-            x[2 * j4 + 1] = __fmul2_rn(make_float2(__uint_as_float(src[2]), __uint_as_float(src[3])),
-                                       make_float2(kq.z, kq.w));
+          for (int i4 = 0; i4 < 4; ++i4) {
+            const float4 kq = *reinterpret_cast<const float4*>(ks + 16 * quad + 4 * i4);
+            ks2[2 * i4] = make_float2(kq.x, kq.y);
+            ks2[2 * i4 + 1] = make_float2(kq.z, kq.w);
+          }
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+#pragma unroll
+            for (int k = 0; k < 2; ++k)
+              x[k][i] = __fmul2_rn(make_float2(__uint_as_float(sv[4 * i + 2 * k]),
+                                               __uint_as_float(sv[4 * i + 2 * k + 1])), ks2[i]);
+          }
+          int nvis[2];
+          bool full = true;
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            nvis[k] = live[k] ? min(kTileKeys, lim[k] - k0 + 1) : 0;
+            full = full && nvis[k] == kTileKeys;
           }
           if (!full) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              if (2 * j >= nvis) x[j].x = -INFINITY;
-              if (2 * j + 1 >= nvis) x[j].y = -INFINITY;
-            }
-          }
-          float mt = -INFINITY;
+            for (int k = 0; k < 2; ++k)
 #pragma unroll
-          for (int j = 0; j < 32; ++j) mt = fmax3(mt, x[j].x, x[j].y);
-          const float m_new = fmaxf(m, mt);
-          float m_use = m;
-          if (m == -INFINITY) {
-            m_use = m_new;
-          } else if (rowfac * (m_new - m) > kRescaleLog2) {
-            alpha = ex2(rowfac * (m - m_new));
-            m_use = m_new;
+              for (int i = 0; i < 8; ++i) {
+                const int j = 16 * quad + 2 * i;
+                if (j >= nvis[k]) x[k][i].x = -INFINITY;
+                if (j + 1 >= nvis[k]) x[k][i].y = -INFINITY;
+              }
           }
-          m = m_use;
-          const float base = (m_use == -INFINITY) ? 0.f : rowfac * m_use;
-          const float2 rf2 = make_float2(rowfac, rowfac), nb2 = make_float2(-base, -base);
-          float2 acc = make_float2(0.f, 0.f);
+          float base[2];
 #pragma unroll
-          for (int j4 = 0; j4 < 16; ++j4) {
-            float4 vq = vs4[j4];
-            if (!full) {      // scales of masked keys are not trusted
-              const int j = 4 * j4;
-              if (j >= nvis) vq.x = 0.f;
-              if (j + 1 >= nvis) vq.y = 0.f;
-              if (j + 2 >= nvis) vq.z = 0.f;
-              if (j + 3 >= nvis) vq.w = 0.f;
+          for (int k = 0; k < 2; ++k) {
+            float mt = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) mt = fmax3(mt, x[k][i].x, x[k][i].y);
+            mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 1));
+            mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 2));
+            const float m_new = fmaxf(m[k], mt);
+            float m_use = m[k];
+            if (m[k] == -INFINITY) {
+              m_use = m_new;
+            } else if (rowfac[k] * (m_new - m[k]) > kRescaleLog2) {
+              alpha[k] = ex2(rowfac[k] * (m[k] - m_new));
+              m_use = m_new;
             }
-            const float2 e0 = __ffma2_rn(x[2 * j4], rf2, nb2);
-            const float2 e1 = __ffma2_rn(x[2 * j4 + 1], rf2, nb2);
-            const float2 p0 = make_float2(ex2(e0.x), ex2(e0.y));
-            const float2 p1 = make_float2(ex2(e1.x), ex2(e1.y));
-            acc = __fadd2_rn(acc, __fadd2_rn(p0, p1));
-            const float2 q0 = __fmul2_rn(p0, make_float2(vq.x, vq.y));
-            const float2 q1 = __fmul2_rn(p1, make_float2(vq.z, vq.w));
-            __half2 h0 = __float22half2_rn(q0), h1 = __float22half2_rn(q1);
-            pw[2 * j4] = *reinterpret_cast<uint32_t*>(&h0);
-            pw[2 * j4 + 1] = *reinterpret_cast<uint32_t*>(&h1);
+            m[k] = m_use;
+            base[k] = (m_use == -INFINITY) ? 0.f : rowfac[k] * m_use;
           }
-          l = l * alpha + (acc.x + acc.y);
+#pragma unroll
+          float2 vs2[8];
+#pragma unroll
+          for (int i4 = 0; i4 < 4; ++i4) {
+            const float4 vq4 = *reinterpret_cast<const float4*>(vs + 16 * quad + 4 * i4);
+            vs2[2 * i4] = make_float2(vq4.x, vq4.y);
+            vs2[2 * i4 + 1] = make_float2(vq4.z, vq4.w);
+          }
+          for (int k = 0; k < 2; ++k) {
+            const float2 rf2 = make_float2(rowfac[k], rowfac[k]);
+            const float2 nb2 = make_float2(-base[k], -base[k]);
+            float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              float2 vq = vs2[i];
+              if (!full) {      // scales of masked keys are not trusted
+                const int j = 16 * quad + 2 * i;
+                if (j >= nvis[k]) vq.x = 0.f;
+                if (j + 1 >= nvis[k]) vq.y = 0.f;
+              }
+              const float2 e0 = __ffma2_rn(x[k][i], rf2, nb2);
+              const float2 p0 = make_float2(ex2(e0.x), ex2(e0.y));
+              acc = __fadd2_rn(acc, p0);
+              __half2 h0 = __float22half2_rn(__fmul2_rn(p0, vq));
+              pw[2 * i + k] = *reinterpret_cast<uint32_t*>(&h0);   // packed column 4i + quad
+            }
+            l[k] = l[k] * alpha[k] + (acc.x + acc.y);
+          }
         }
         // a rescale of O waits for the previous tile's PV (rare: the running
         // max is only moved when it grows by more than 2^8). p_free of that
         // tile's buffer: its previous phase (PV three tiles back) is complete,
         // so a parity wait cannot be satisfied by an older phase.
-        if (it > s.i0 && warp_live && __any_sync(0xffffffffu, alpha != 1.f)) {
+        if (it > s.i0 && warp_live &&
+            __any_sync(0xffffffffu, alpha[0] != 1.f || alpha[1] != 1.f)) {
           ok = sync.wait(smem_u32(&sh->p_free[(g - 1) % kStages]), ((g - 1) / kStages) & 1);
           if (!ok) break;
           fence_after();
 #pragma unroll 1
-          for (int c0 = 0; c0 < D; c0 += 32) {
+          for (int c0 = 0; c0 < D; c0 += 64) {
             uint32_t v[32];
-            tmem_ld32(tmem + lane_base + C::kOCol + c0, v);
+            tmem_ld16x256_x8(tmem + lane_base + C::kOCol + c0, v);
             tmem_wait_ld();
 #pragma unroll
-            for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * alpha);
-            tmem_st32(tmem + lane_base + C::kOCol + c0, v);
+            for (int i = 0; i < 8; ++i)
+#pragma unroll
+              for (int k = 0; k < 2; ++k) {
+                v[4 * i + 2 * k] = __float_as_uint(__uint_as_float(v[4 * i + 2 * k]) * alpha[k]);
+                v[4 * i + 2 * k + 1] =
+                    __float_as_uint(__uint_as_float(v[4 * i + 2 * k + 1]) * alpha[k]);
+              }
+            tmem_st16x256_x8(tmem + lane_base + C::kOCol + c0, v);
           }
         }
         if (warp_live) {
-          tmem_st32(tmem + lane_base + C::kSCol + st * kTileKeys, pw);
+          tmem_st16x128_x16(tmem + lane_base + C::kSCol + st * kTileKeys, pw);
           tmem_wait_st();
         }
         fence_before();
@@ -593,45 +713,46 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
       fence_after();
       if (warp_live) {
         const int ns = nseg[s.u];
-        const long long prow = (long long)part_base[s.u] +
-                               (long long)(blockIdx.x - cfirst[s.u]) * s.R + r;
-        const float inv = l > 0.f ? 1.f / l : 0.f;
-        const size_t orow = ((size_t)(q_off[s.b] + tt) * p.num_q_heads + s.h * G + gg);
+        float inv[2];
+        long long prow[2];
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          float lt = l[k];
+          lt += __shfl_xor_sync(0xffffffffu, lt, 1);
+          lt += __shfl_xor_sync(0xffffffffu, lt, 2);
+          l[k] = lt;
+          inv[k] = lt > 0.f ? 1.f / lt : 0.f;
+          prow[k] = (long long)part_base[s.u] + (long long)(blockIdx.x - cfirst[s.u]) * s.R + rr[k];
+        }
 #pragma unroll 1
-        for (int c0 = 0; c0 < D; c0 += 32) {
+        for (int c0 = 0; c0 < D; c0 += 64) {
           uint32_t v[32];
-          tmem_ld32(tmem + lane_base + C::kOCol + c0, v);
+          tmem_ld16x256_x8(tmem + lane_base + C::kOCol + c0, v);
           tmem_wait_ld();
-          if (row_live) {
-            if (ns == 1) {
-              __nv_bfloat16* dst = p.out + orow * D + c0;
 #pragma unroll
-              for (int k = 0; k < 32; k += 8) {
-                uint4 w;
-                __nv_bfloat162 b0 = __floats2bfloat162_rn(__uint_as_float(v[k]) * inv, __uint_as_float(v[k + 1]) * inv);
-                __nv_bfloat162 b1 = __floats2bfloat162_rn(__uint_as_float(v[k + 2]) * inv, __uint_as_float(v[k + 3]) * inv);
-                __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(v[k + 4]) * inv, __uint_as_float(v[k + 5]) * inv);
-                __nv_bfloat162 b3 = __floats2bfloat162_rn(__uint_as_float(v[k + 6]) * inv, __uint_as_float(v[k + 7]) * inv);
-                w.x = *reinterpret_cast<uint32_t*>(&b0);
-                w.y = *reinterpret_cast<uint32_t*>(&b1);
-                w.z = *reinterpret_cast<uint32_t*>(&b2);
-                w.w = *reinterpret_cast<uint32_t*>(&b3);
-                *reinterpret_cast<uint4*>(dst + k) = w;
-              }
-            } else {
-              float* dst = o_part + prow * D + c0;
+          for (int k = 0; k < 2; ++k) {
+            if (!live[k]) continue;
 #pragma unroll
-              for (int k = 0; k < 32; k += 4)
-                *reinterpret_cast<float4*>(dst + k) =
-                    make_float4(__uint_as_float(v[k]) * inv, __uint_as_float(v[k + 1]) * inv,
-                                __uint_as_float(v[k + 2]) * inv, __uint_as_float(v[k + 3]) * inv);
+            for (int i = 0; i < 8; ++i) {
+              const int d = c0 + 8 * i + 2 * quad;
+              const float o0 = __uint_as_float(v[4 * i + 2 * k]) * inv[k];
+              const float o1 = __uint_as_float(v[4 * i + 2 * k + 1]) * inv[k];
+              if (ns == 1)
+                *reinterpret_cast<__nv_bfloat162*>(p.out + qrow_off[k] * D + d) =
+                    __floats2bfloat162_rn(o0, o1);
+              else
+                *reinterpret_cast<float2*>(o_part + prow[k] * D + d) = make_float2(o0, o1);
             }
           }
         }
-        if (row_live) {
-          const float lse = l > 0.f ? (rowfac * m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
-          if (ns == 1) p.lse[orow] = lse;
-          else lse_part[prow] = lse;
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          if (live[k] && quad == 0) {
+            const float lse =
+                l[k] > 0.f ? (rowfac[k] * m[k] + __log2f(l[k])) * 0.69314718055994531f : -INFINITY;
+            if (ns == 1) p.lse[qrow_off[k]] = lse;
+            else lse_part[prow[k]] = lse;
+          }
         }
       }
       fence_before();
@@ -664,6 +785,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
     int g = 0;
     Seg s;
     bool ok = true;
+    PageWindow win;
     while (ok && iter.next(s)) {
       for (int it = s.i0; it < s.i1; ++it, ++g) {
         const int r = g % kRing, vst = g % kVStages;
@@ -675,7 +797,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
         stage_tile<D>(p, s, it, ring + r * C::kRingStage, scales + vst * 2 * kTileKeys,
-                      smem_u32(&sh->ring_full[r]), smem_u32(&sh->sc_full[vst]), lane);
+                      smem_u32(&sh->ring_full[r]), smem_u32(&sh->sc_full[vst]), lane, win);
       }
     }
   } else {
@@ -683,13 +805,9 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
     if (lane == 0) {
       constexpr uint32_t kIdescQK = idesc_f16(128, kTileKeys, 0);
       constexpr uint32_t kIdescPV = idesc_f16(128, D, 1);
-      // descriptors of k-step 0 of every buffer; k-steps add byte offsets >> 4
-      uint64_t kdesc[kStages], vdesc[kVStages];
-#pragma unroll
-      for (int i = 0; i < kStages; ++i) kdesc[i] = sdesc(smem_u32(kbuf + i * C::kTileBytes), 16, 1024);
-#pragma unroll
-      for (int i = 0; i < kVStages; ++i)
-        vdesc[i] = sdesc(smem_u32(vbuf + i * C::kTileBytes), kTileKeys * 128, 1024);
+      // descriptors of k-step 0 of buffer 0; buffers and k-steps add byte offsets >> 4
+      const uint64_t kdesc0 = sdesc(smem_u32(kbuf), 16, 1024);
+      const uint64_t vdesc0 = sdesc(smem_u32(vbuf), kTileKeys * 128, 1024);
       int g = 0, nsegs = 0;
       Seg s;
       bool ok = true;
@@ -705,33 +823,40 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
         // complete (p_free).
         int nq = 0, np = 0;
         unsigned long long t_idle = 0;
+        uint32_t idle_polls = 0;
+        auto try_pv = [&]() -> bool {
+          if (np >= nq) return false;
+          const int gi = g + np, st = gi % kStages, vst = gi % kVStages;
+          if (!mbar_test_wait(smem_u32(&sh->p_full[st]), (gi / kStages) & 1)) return false;
+          fence_after();
+#pragma unroll
+          for (int kk = 0; kk < kTileKeys / 16; ++kk)
+            mma_ts(tmem + C::kOCol, tmem + C::kSCol + st * kTileKeys + kk * 8,
+                   vdesc0 + (uint64_t)((vst * C::kTileBytes + kk * 16 * 128) >> 4), kIdescPV,
+                   (np == 0 && kk == 0) ? 0u : 1u);
+          mma_commit(smem_u32(&sh->v_free[vst]));
+          mma_commit(smem_u32(&sh->p_free[st]));
+          ++np;
+          return true;
+        };
         while (np < n) {
           bool progressed = false;
-          if (np < nq) {
-            const int gi = g + np, st = gi % kStages, vst = gi % kVStages;
-            if (mbar_test_wait(smem_u32(&sh->p_full[st]), (gi / kStages) & 1)) {
-              fence_after();
-#pragma unroll
-              for (int kk = 0; kk < kTileKeys / 16; ++kk)
-                mma_ts(tmem + C::kOCol, tmem + C::kSCol + st * kTileKeys + kk * 8,
-                       vdesc[vst] + (uint64_t)((kk * 16 * 128) >> 4), kIdescPV,
-                       (np == 0 && kk == 0) ? 0u : 1u);
-              mma_commit(smem_u32(&sh->v_free[vst]));
-              mma_commit(smem_u32(&sh->p_free[st]));
-              ++np;
-              progressed = true;
-            }
-          }
+          if (try_pv()) progressed = true;
           if (nq < n && nq <= np + 1) {
             const int gi = g + nq, st = gi % kStages;
             if (mbar_test_wait(smem_u32(&sh->p_free[st]), ((gi / kStages) & 1) ^ 1) &&
                 mbar_test_wait(smem_u32(&sh->kv_full[st]), (gi / kStages) & 1)) {
               fence_after();
 #pragma unroll
-              for (int kk = 0; kk < D / 16; ++kk)
+              for (int kk = 0; kk < D / 16; ++kk) {
                 mma_ts(tmem + C::kSCol + st * kTileKeys, tmem + C::kQCol + kk * 8,
-                       kdesc[st] + (uint64_t)(((kk / 4) * (kTileKeys * 128) + (kk % 4) * 32) >> 4),
+                       kdesc0 + (uint64_t)((st * C::kTileBytes + (kk / 4) * (kTileKeys * 128) +
+                                            (kk % 4) * 32) >> 4),
                        kIdescQK, kk > 0);
+                // a PV that became ready meanwhile goes in between (it reads
+                // the other S/P buffer and accumulates into O)
+                if ((kk & 3) == 3 && kk + 1 < D / 16) try_pv();
+              }
               mma_commit(smem_u32(&sh->s_full[st]));
               mma_commit(smem_u32(&sh->k_free[st]));
               ++nq;
@@ -740,7 +865,8 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
           }
           if (progressed) {
             t_idle = 0;
-          } else {
+            idle_polls = 0;
+          } else if ((++idle_polls & 63) == 0) {     // the timer is read every 64 idle polls
             if (sh->abort_flag) { ok = false; break; }
             const unsigned long long now = global_ns();
             if (t_idle == 0) {
