@@ -183,6 +183,45 @@ int splash_verify_attention_profiled(const uint16_t* q, int num_q_tokens,
                                      struct CUstream_st* stream, int path, int ctas_per_class,
                                      struct CUevent_st* attn_begin, struct CUevent_st* attn_end);
 
+/*
+ * splash_verify_attention_fixed_scratch — splash_verify_attention without a
+ * caller-provided workspace, for callers that cannot allocate device memory:
+ * for example code that runs under a memory manager owning every device
+ * allocation, a plugin whose host forbids allocation calls, or a serving
+ * loop that cannot afford the implicit device synchronisation of cudaMalloc.
+ * (The source pages describe nothing like it; it is a packaging of the same
+ * operation.)
+ *
+ * The workspace is instead a fixed 64 MiB array (see
+ * splash_verify_attention_fixed_scratch_bytes) that is part of this library's
+ * device image: every GPU that loads the library holds it until the process
+ * exits. Nothing is allocated or freed by the call; no allocating library
+ * routine is used. The first call on a device looks up the array's device
+ * address (cudaGetSymbolAddress), so make that first call before any stream
+ * capture. All calls on a device share the one array, which keeps the last
+ * call's contents; the planner rewrites everything a call reads, so nothing
+ * needs clearing between calls. Calls that can overlap on the same GPU (issued
+ * on different streams, or from different host threads) race on the array and
+ * must be serialised by the caller.
+ *
+ * Same arguments, results and errors as splash_verify_attention minus the
+ * workspace, with one CTA per SM for each attention kernel. Returns
+ * SPLASH_ERR_WORKSPACE_TOO_SMALL when the shape needs more scratch than the
+ * fixed array holds (for D = 256 that is beyond about T*G = 105 rows per
+ * sequence on a 152-SM GB300).
+ */
+size_t splash_verify_attention_fixed_scratch_bytes(void);
+int splash_verify_attention_fixed_scratch(const uint16_t* q, int num_q_tokens,
+                                          const int8_t* k_pages, const int8_t* v_pages,
+                                          const float* k_scales, const float* v_scales,
+                                          const int32_t* page_table, int max_pages_per_seq,
+                                          const int32_t* context_lens, const int32_t* block_lens,
+                                          int num_seqs, int num_q_heads, int num_kv_heads,
+                                          int head_dim, int page_size, int num_pages,
+                                          int max_block_len, float sm_scale, uint16_t* out,
+                                          float* lse, int* device_status,
+                                          struct CUstream_st* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -248,3 +248,61 @@ int splash_verify_attention(const uint16_t* q, int num_q_tokens, const int8_t* k
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Entry point for callers that cannot allocate device memory: the workspace is
+// a fixed array in the library's own device image instead of caller memory.
+// ---------------------------------------------------------------------------
+namespace {
+constexpr size_t kFixedScratchBytes = size_t(64) << 20;   // 64 MiB per device
+}  // namespace
+
+// Lives in every device image that loads this library, until the process exits.
+static __device__ __align__(256) unsigned char g_fixed_scratch[kFixedScratchBytes];
+
+namespace {
+std::mutex g_fixed_mu;
+void* g_fixed_ptr[64] = {};
+
+// Device address of g_fixed_scratch on the current device, looked up once per
+// device (host code only sees a host-side stand-in under that name).
+void* fixed_scratch_current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(g_fixed_mu);
+  if (g_fixed_ptr[dev] == nullptr) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_fixed_scratch) != cudaSuccess) return nullptr;
+    g_fixed_ptr[dev] = ptr;
+  }
+  return g_fixed_ptr[dev];
+}
+}  // namespace
+
+extern "C" size_t splash_verify_attention_fixed_scratch_bytes(void) { return kFixedScratchBytes; }
+
+extern "C" int splash_verify_attention_fixed_scratch(
+    const uint16_t* q, int num_q_tokens, const int8_t* k_pages, const int8_t* v_pages,
+    const float* k_scales, const float* v_scales, const int32_t* page_table,
+    int max_pages_per_seq, const int32_t* context_lens, const int32_t* block_lens, int num_seqs,
+    int num_q_heads, int num_kv_heads, int head_dim, int page_size, int num_pages,
+    int max_block_len, float sm_scale, uint16_t* out, float* lse, int* device_status,
+    struct CUstream_st* stream) {
+  const int st = check_attn_shape(num_q_tokens, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                  page_size, max_block_len, max_pages_per_seq);
+  if (st != SPLASH_OK) return st;
+  if (num_q_tokens == 0 || num_seqs == 0 || max_block_len == 0) return SPLASH_OK;
+  const int sms = device_sm_count();
+  if (sms <= 0) return SPLASH_ERR_CUDA;
+  // one CTA per SM for each kernel keeps the partial-row bound small
+  const size_t need = workspace_bytes_for(num_seqs, num_q_tokens, num_q_heads, num_kv_heads,
+                                          head_dim, max_block_len, sms, sms);
+  if (need > kFixedScratchBytes) return SPLASH_ERR_WORKSPACE_TOO_SMALL;
+  void* scratch = fixed_scratch_current_device();
+  if (scratch == nullptr) return SPLASH_ERR_CUDA;
+  return splash_verify_attention_tuned(q, num_q_tokens, k_pages, v_pages, k_scales, v_scales,
+                                       page_table, max_pages_per_seq, context_lens, block_lens,
+                                       num_seqs, num_q_heads, num_kv_heads, head_dim, page_size,
+                                       num_pages, max_block_len, sm_scale, out, lse, scratch,
+                                       kFixedScratchBytes, device_status, stream, 0, sms);
+}

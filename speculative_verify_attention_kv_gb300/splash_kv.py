@@ -50,6 +50,10 @@ def _load() -> ctypes.CDLL:
     lib.splash_verify_attention_tuned.argtypes = attn + [I, I]
     lib.splash_verify_attention_profiled.restype = I
     lib.splash_verify_attention_profiled.argtypes = attn + [I, I, P, P]
+    lib.splash_verify_attention_fixed_scratch_bytes.restype = S
+    lib.splash_verify_attention_fixed_scratch_bytes.argtypes = []
+    lib.splash_verify_attention_fixed_scratch.restype = I
+    lib.splash_verify_attention_fixed_scratch.argtypes = attn[:20] + [P, P]
     return lib
 
 
@@ -57,7 +61,8 @@ LIB = _load()
 EXPORTED = ("splash_status_string", "splash_abi_version", "splash_tensor_path_supported",
             "splash_kv_append",
             "splash_verify_attention_workspace_size", "splash_verify_attention",
-            "splash_verify_attention_tuned", "splash_verify_attention_profiled")
+            "splash_verify_attention_tuned", "splash_verify_attention_profiled",
+            "splash_verify_attention_fixed_scratch_bytes", "splash_verify_attention_fixed_scratch")
 
 
 def tensor_path_available(head_dim: int) -> bool:
@@ -181,3 +186,34 @@ def splash_verify_attention(q, k_pages, v_pages, k_scales, v_scales, page_table,
         st = LIB.splash_verify_attention_tuned(*args, int(path), int(ctas_per_class))
     if st != 0:
         raise SplashError(st, "splash_verify_attention")
+
+
+def splash_verify_attention_fixed_scratch(q, k_pages, v_pages, k_scales, v_scales, page_table,
+                                          context_lens, block_lens, sm_scale: float,
+                                          max_block_len: int, out, lse, device_status=None,
+                                          stream=None) -> None:
+    """splash_verify_attention with the library's fixed device scratch instead
+    of a workspace (for callers that cannot allocate device memory)."""
+    _check(q, "q", torch.bfloat16, 3)
+    _check(out, "out", torch.bfloat16, 3)
+    _check(lse, "lse", torch.float32, 2)
+    for n, t in (("k_pages", k_pages), ("v_pages", v_pages)):
+        _check(t, n, torch.int8, 4)
+    for n, t in (("k_scales", k_scales), ("v_scales", v_scales)):
+        _check(t, n, torch.float32, 3)
+    _check(page_table, "page_table", torch.int32, 2)
+    _check(context_lens, "context_lens", torch.int32, 1)
+    _check(block_lens, "block_lens", torch.int32, 1)
+    if device_status is not None:
+        _check(device_status, "device_status", torch.int32)
+    num_pages, hkv, P, D = k_pages.shape
+    n_tok, hq, dq = q.shape
+    if dq != D or tuple(out.shape) != tuple(q.shape) or tuple(lse.shape) != (n_tok, hq):
+        raise ValueError("shape mismatch between q, out, lse and the pool")
+    st = LIB.splash_verify_attention_fixed_scratch(
+        _ptr(q), n_tok, _ptr(k_pages), _ptr(v_pages), _ptr(k_scales), _ptr(v_scales),
+        _ptr(page_table), page_table.shape[1], _ptr(context_lens), _ptr(block_lens),
+        context_lens.shape[0], hq, hkv, D, P, num_pages, int(max_block_len), float(sm_scale),
+        _ptr(out), _ptr(lse), _ptr(device_status), _stream(stream))
+    if st != 0:
+        raise SplashError(st, "splash_verify_attention_fixed_scratch")
