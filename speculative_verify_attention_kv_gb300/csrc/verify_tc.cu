@@ -15,14 +15,17 @@
 // are exact in fp16). The K scale multiplies score columns, the V scale is
 // folded into P before P is rounded to fp16.
 //
-// Warp roles (448 threads):
+// Warp roles (512 threads):
 //   warps 0-7   softmax + epilogue: warp w owns TMEM lanes (rows) 32(w%4) +
 //               16(w/4) .. +15; with the 16x256b load shape each row is spread
 //               over 4 threads (2 rows per thread, row reductions = 2 shuffles)
 //   warps 8-11  converters: int8 codes from the staging ring -> fp16 in
 //               registers -> 128B-swizzled SMEM tiles (K: K-major, V: MN-major)
-//   warp  12    TMEM allocation and the single MMA-issuing thread
-//   warp  13    producer: bulk async copies (TMA, untiled) of whole
+//   warp  12    TMEM allocation; one thread issues the QK MMAs
+//   warp  13    one thread issues the PV MMAs (two issuing threads keep the
+//               tensor pipe fed better than one)
+//   warps 14-15 producers, one per staging-ring stage (even / odd tiles):
+//               bulk async copies (TMA, untiled) of whole
 //               (page, KV head) blocks: codes into a 2-stage int8 staging
 //               ring ahead of the converters, scales straight into the
 //               3-stage scale arrays the softmax reads
@@ -43,9 +46,10 @@ constexpr int kRing = 2;                      // int8 staging stages
 constexpr int kSoftmaxWarps = 8;              // 2 per TMEM lane quarter, 16 rows each
 constexpr int kLoadWarps = 4;
 constexpr int kLoadThreads = 32 * kLoadWarps;
-constexpr int kMmaWarp = kSoftmaxWarps + kLoadWarps;
-constexpr int kProducerWarp = kMmaWarp + 1;
-constexpr int kThreads = 32 * (kProducerWarp + 1);
+constexpr int kMmaWarp = kSoftmaxWarps + kLoadWarps;   // TMEM allocation, QK issue
+constexpr int kPvWarp = kMmaWarp + 1;                   // PV issue
+constexpr int kProducerWarp = kPvWarp + 1;              // first of kRing producer warps
+constexpr int kThreads = 32 * (kProducerWarp + kRing);
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.0f;          // lazy rescale threshold (factor 256)
 constexpr unsigned long long kWaitNs = 1000000000ull;
@@ -288,7 +292,8 @@ struct SegIter {
 struct Smem {
   uint64_t ring_full[kRing];      // producer tx -> converters
   uint64_t ring_empty[kRing];     // converters -> producer
-  uint64_t sc_full[kVStages];     // producer tx (scales) -> softmax
+  uint64_t sc_full[kVStages];     // producer cp.async (scales) -> softmax
+  uint64_t sc_free[kVStages];     // softmax done with the scales -> producer
   uint64_t kv_full[kStages];      // converters -> MMA (fp16 K and V of the tile ready)
   uint64_t k_free[kStages];       // QK done -> converters
   uint64_t v_free[kVStages];      // PV done -> converters, producer (scales)
@@ -297,7 +302,7 @@ struct Smem {
   uint64_t p_free[kStages];       // PV of the buffer's tile done -> MMA (QK may
                                   // overwrite the S/P buffer), softmax (O rescale, epilogue)
   uint64_t q_full;                // softmax (Q' in TMEM) -> MMA
-  uint64_t drain;
+  uint64_t drain[2];              // QK / PV issuer: all of its MMAs complete
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -481,10 +486,12 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
     }
     for (int s = 0; s < kVStages; ++s) {
       mbar_init(smem_u32(&sh->sc_full[s]), 32);     // one cp.async arrival per producer lane
+      mbar_init(smem_u32(&sh->sc_free[s]), 32 * kSoftmaxWarps);
       mbar_init(smem_u32(&sh->v_free[s]), 1);
     }
     mbar_init(smem_u32(&sh->q_full), 32 * kSoftmaxWarps);
-    mbar_init(smem_u32(&sh->drain), 1);
+    mbar_init(smem_u32(&sh->drain[0]), 1);
+    mbar_init(smem_u32(&sh->drain[1]), 1);
     sh->abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -699,6 +706,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
             tmem_st16x256_x8(tmem + lane_base + C::kOCol + c0, v);
           }
         }
+        mbar_arrive(smem_u32(&sh->sc_free[vst]));          // scales of this tile are read
         if (warp_live) {
           tmem_st16x128_x16(tmem + lane_base + C::kSCol + st * kTileKeys, pw);
           tmem_wait_st();
@@ -780,8 +788,10 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
         mbar_arrive(smem_u32(&sh->kv_full[st]));
       }
     }
-  } else if (warp == kProducerWarp) {
-    // ============================================================ producer
+  } else if (warp >= kProducerWarp) {
+    // =========================================================== producers
+    // producer warp `mine` stages the tiles of ring stage `mine` (g % kRing)
+    const int mine = warp - kProducerWarp;
     int g = 0;
     Seg s;
     bool ok = true;
@@ -789,10 +799,12 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
     while (ok && iter.next(s)) {
       for (int it = s.i0; it < s.i1; ++it, ++g) {
         const int r = g % kRing, vst = g % kVStages;
+        if (r != mine) continue;
         if (lane == 0) {
-          // ring stage free (converted), scale stage free (PV three tiles back done)
+          // ring stage free (converted), scale stage free (read by the softmax
+          // of the tile three back)
           ok = sync.wait(smem_u32(&sh->ring_empty[r]), ((g / kRing) & 1) ^ 1) &&
-               sync.wait(smem_u32(&sh->v_free[vst]), ((g / kVStages) & 1) ^ 1);
+               sync.wait(smem_u32(&sh->sc_free[vst]), ((g / kVStages) & 1) ^ 1);
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
@@ -801,7 +813,12 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
       }
     }
   } else {
-    // ================================================================= MMA
+    // ============================================================ MMA issue
+    // warp kMmaWarp: QK(i) into S[i % 2] once its K tile is converted and the
+    // PV that last read that S/P buffer (tile i - 2) has completed (issue order
+    // alone does not order a later TMEM write after an earlier MMA's read).
+    // warp kPvWarp: PV(i) into O once the softmax has written P(i).
+    const bool is_qk = warp == kMmaWarp;
     if (lane == 0) {
       constexpr uint32_t kIdescQK = idesc_f16(128, kTileKeys, 0);
       constexpr uint32_t kIdescPV = idesc_f16(128, D, 1);
@@ -812,79 +829,44 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
       Seg s;
       bool ok = true;
       while (ok && iter.next(s)) {
-        ok = sync.wait(smem_u32(&sh->q_full), nsegs & 1);
-        if (!ok) break;
-        fence_after();
-        const int n = s.i1 - s.i0;
-        // PV(i) and QK(i) are issued in their own orders, each as soon as its
-        // inputs are ready (PV first: it frees V buffers). QK(i) overwrites the
-        // S/P buffer that PV(i-2) reads as its A operand: issue order does not
-        // order that write after the read, so QK(i) waits for PV(i-2) to
-        // complete (p_free).
-        int nq = 0, np = 0;
-        unsigned long long t_idle = 0;
-        uint32_t idle_polls = 0;
-        auto try_pv = [&]() -> bool {
-          if (np >= nq) return false;
-          const int gi = g + np, st = gi % kStages, vst = gi % kVStages;
-          if (!mbar_test_wait(smem_u32(&sh->p_full[st]), (gi / kStages) & 1)) return false;
+        if (is_qk) {
+          ok = sync.wait(smem_u32(&sh->q_full), nsegs & 1);
+          if (!ok) break;
           fence_after();
+        }
+        for (int it = s.i0; it < s.i1 && ok; ++it, ++g) {
+          const int st = g % kStages, vst = g % kVStages;
+          if (is_qk) {
+            ok = sync.wait(smem_u32(&sh->p_free[st]), ((g / kStages) & 1) ^ 1) &&
+                 sync.wait(smem_u32(&sh->kv_full[st]), (g / kStages) & 1);
+            if (!ok) break;
+            fence_after();
 #pragma unroll
-          for (int kk = 0; kk < kTileKeys / 16; ++kk)
-            mma_ts(tmem + C::kOCol, tmem + C::kSCol + st * kTileKeys + kk * 8,
-                   vdesc0 + (uint64_t)((vst * C::kTileBytes + kk * 16 * 128) >> 4), kIdescPV,
-                   (np == 0 && kk == 0) ? 0u : 1u);
-          mma_commit(smem_u32(&sh->v_free[vst]));
-          mma_commit(smem_u32(&sh->p_free[st]));
-          ++np;
-          return true;
-        };
-        while (np < n) {
-          bool progressed = false;
-          if (try_pv()) progressed = true;
-          if (nq < n && nq <= np + 1) {
-            const int gi = g + nq, st = gi % kStages;
-            if (mbar_test_wait(smem_u32(&sh->p_free[st]), ((gi / kStages) & 1) ^ 1) &&
-                mbar_test_wait(smem_u32(&sh->kv_full[st]), (gi / kStages) & 1)) {
-              fence_after();
+            for (int kk = 0; kk < D / 16; ++kk)
+              mma_ts(tmem + C::kSCol + st * kTileKeys, tmem + C::kQCol + kk * 8,
+                     kdesc0 + (uint64_t)((st * C::kTileBytes + (kk / 4) * (kTileKeys * 128) +
+                                          (kk % 4) * 32) >> 4),
+                     kIdescQK, kk > 0);
+            mma_commit(smem_u32(&sh->s_full[st]));
+            mma_commit(smem_u32(&sh->k_free[st]));
+          } else {
+            ok = sync.wait(smem_u32(&sh->p_full[st]), (g / kStages) & 1);
+            if (!ok) break;
+            fence_after();
 #pragma unroll
-              for (int kk = 0; kk < D / 16; ++kk) {
-                mma_ts(tmem + C::kSCol + st * kTileKeys, tmem + C::kQCol + kk * 8,
-                       kdesc0 + (uint64_t)((st * C::kTileBytes + (kk / 4) * (kTileKeys * 128) +
-                                            (kk % 4) * 32) >> 4),
-                       kIdescQK, kk > 0);
-                // a PV that became ready meanwhile goes in between (it reads
-                // the other S/P buffer and accumulates into O)
-                if ((kk & 3) == 3 && kk + 1 < D / 16) try_pv();
-              }
-              mma_commit(smem_u32(&sh->s_full[st]));
-              mma_commit(smem_u32(&sh->k_free[st]));
-              ++nq;
-              progressed = true;
-            }
-          }
-          if (progressed) {
-            t_idle = 0;
-            idle_polls = 0;
-          } else if ((++idle_polls & 63) == 0) {     // the timer is read every 64 idle polls
-            if (sh->abort_flag) { ok = false; break; }
-            const unsigned long long now = global_ns();
-            if (t_idle == 0) {
-              t_idle = now;
-            } else if (now - t_idle > kWaitNs) {
-              sh->abort_flag = 1;
-              report(p.device_status, SPLASH_DEVICE_TIMEOUT);
-              ok = false;
-              break;
-            }
+            for (int kk = 0; kk < kTileKeys / 16; ++kk)
+              mma_ts(tmem + C::kOCol, tmem + C::kSCol + st * kTileKeys + kk * 8,
+                     vdesc0 + (uint64_t)((vst * C::kTileBytes + kk * 16 * 128) >> 4), kIdescPV,
+                     (it == s.i0 && kk == 0) ? 0u : 1u);
+            mma_commit(smem_u32(&sh->v_free[vst]));
+            mma_commit(smem_u32(&sh->p_free[st]));
           }
         }
-        g += n;
         ++nsegs;
       }
-      // every MMA issued so far is complete before TMEM is released
-      mma_commit(smem_u32(&sh->drain));
-      sync.wait(smem_u32(&sh->drain), 0);
+      // every MMA this thread issued is complete before TMEM is released
+      mma_commit(smem_u32(&sh->drain[is_qk ? 0 : 1]));
+      sync.wait(smem_u32(&sh->drain[is_qk ? 0 : 1]), 0);
     }
     __syncwarp();
   }
