@@ -371,10 +371,9 @@ def run_ours(args):
 def dw_launches_per_step(W: wl.Workload, path: int) -> int:
     """Kernels one step launches: append, planner, attention kernel(s), combine."""
     from speculative_verify_attention_kv_gb300 import splash_kv as sk
-    tc = sk.tensor_path_available(W.spec.head_dim)
-    # automatic mode with the tensor-core kernel launches both kernels (one may find no work)
-    n_attn = 2 if (path == 0 and tc) else 1
-    return 1 + 1 + n_attn + 1
+    # one attention kernel: the tensor-core kernel takes every unit in automatic
+    # mode when it exists for the head size, else the CUDA-core kernel
+    return 1 + 1 + 1 + 1
 
 
 def main(argv=None):

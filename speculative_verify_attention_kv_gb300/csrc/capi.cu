@@ -155,8 +155,10 @@ int splash_verify_attention_profiled(
   const bool tc_ok = tc_supported(head_dim);
   if (path == 2 && !tc_ok) return SPLASH_ERR_UNSUPPORTED;
   if (!tc_ok) path = 1;
-  // rows the CUDA-core kernel may see: all (path 1), none (path 2), < 16 (automatic)
-  const int rows_simt = path == 1 ? rows_cap : path == 2 ? 0 : (rows_cap < 15 ? rows_cap : 15);
+  // rows the CUDA-core kernel may see: all (path 1), none (path 2), fewer than
+  // kTensorMinRows (automatic)
+  const int rows_simt = path == 1 ? rows_cap : path == 2 ? 0
+                        : (rows_cap < kTensorMinRows - 1 ? rows_cap : kTensorMinRows - 1);
   // the CUDA-core kernel holds every row of a unit in shared memory
   if (rows_simt > 0 && simt_smem_bytes(head_dim, rows_simt) > 227 * 1024)
     return SPLASH_ERR_UNSUPPORTED;
@@ -205,7 +207,7 @@ int splash_verify_attention_profiled(
     e = launch_verify_tc(p, rows_cap, nt, s);
     if (e != cudaSuccess) return SPLASH_ERR_CUDA;
   }
-  if (path != 2) {
+  if (path != 2 && rows_simt > 0) {
     e = launch_verify_simt(p, rows_simt, ns, s);
     if (e != cudaSuccess) return SPLASH_ERR_CUDA;
   }

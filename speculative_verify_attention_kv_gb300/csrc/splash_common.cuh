@@ -15,6 +15,12 @@ constexpr int kClassTensor = 0;   // sequences whose T*G rows go to the tensor-c
 constexpr int kClassSimt = 1;     // sequences whose rows go to the CUDA-core kernel
 constexpr int kNumClasses = 2;
 constexpr int kMaxRows = 128;     // T*G limit per sequence and KV head
+// Automatic routing: units with at least this many query rows go to the
+// tensor-core kernel. Its cost per key tile does not depend on the row count
+// (rows are padded to 128), and measured on a ragged batch (T in {1,4,8,16},
+// G = 6) it beats the CUDA-core kernel even at T*G = 6, so every unit goes
+// there when a tensor-core kernel exists for the head size.
+constexpr int kTensorMinRows = 1;
 
 // Plan written by the planner kernel at the start of the workspace.
 struct PlanHeader {

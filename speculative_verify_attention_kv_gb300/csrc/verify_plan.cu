@@ -77,7 +77,7 @@ plan_kernel(const int32_t* __restrict__ context_lens, const int32_t* __restrict_
       if (T > 0) {
         const int rows = T * group;
         cls = path == 1 ? kClassSimt : path == 2 ? kClassTensor
-                        : (rows >= 16 ? kClassTensor : kClassSimt);
+                        : (rows >= kTensorMinRows ? kClassTensor : kClassSimt);
         tiles = (ctx + T + tile[cls] - 1) / tile[cls];
       }
       seq_T[b] = T;
