@@ -108,6 +108,41 @@ int splash_kv_append(const float* k_new, const float* v_new, int num_new_tokens,
                      int* device_status, struct CUstream_st* stream);
 
 /*
+ * splash_kv_append_bf16 — splash_kv_append for bf16 K/V rows (bit patterns,
+ * [num_new_tokens, Hkv, D]), the dtype a projection usually produces. Each
+ * value converts exactly to fp32, then the same quantiser applies; codes and
+ * scales equal those of splash_kv_append on the fp32 copies of the same rows.
+ */
+int splash_kv_append_bf16(const uint16_t* k_new, const uint16_t* v_new, int num_new_tokens,
+                          int8_t* k_pages, int8_t* v_pages, float* k_scales, float* v_scales,
+                          const int32_t* page_table, int max_pages_per_seq,
+                          const int32_t* context_lens, const int32_t* block_lens, int num_seqs,
+                          int num_kv_heads, int head_dim, int page_size, int num_pages,
+                          int* device_status, struct CUstream_st* stream);
+
+/*
+ * splash_accept_commit — the step after verification: each sequence advances
+ * by the tokens it accepted (Splash article, section "옵션이 아니라 기본 경로인
+ * DFlash 2 추측 디코딩": every request carries its own draft state and moves on
+ * by its accepted tokens).
+ *
+ * block_tokens, target_tokens: int32 [num_tokens], packed by sequence like q.
+ * Sequence b's block is x_0 .. x_{T_b-1} (x_0 = the token the target emitted at
+ * the previous step, x_1.. = the draft's proposals); target_tokens holds the
+ * target's next-token choice y_i after each x_i. Draft x_{i+1} is accepted
+ * while x_{i+1} == y_i for all earlier i. With a accepted drafts:
+ *   accepted[b] = a;  context_lens[b] += a + 1 (x_0 .. x_a are committed: their
+ *   K/V were written by the block append);  next_tokens[b] = y_a.
+ * Sequences with T_b = 0 get accepted = 0, next_tokens = -1 and keep their
+ * length. Slots beyond the new length are overwritten by the next append.
+ * context_lens is updated in place on the device; one small launch, no sync.
+ */
+int splash_accept_commit(const int32_t* block_tokens, const int32_t* target_tokens,
+                         int num_tokens, const int32_t* block_lens, int32_t* context_lens,
+                         int32_t* accepted, int32_t* next_tokens, int num_seqs,
+                         int* device_status, struct CUstream_st* stream);
+
+/*
  * splash_verify_attention_workspace_size — bytes of device workspace that
  * splash_verify_attention needs for these bounds on the current device
  * (depends on its SM count). Returns 0 for invalid arguments.

@@ -37,6 +37,11 @@ here (the same ones the CUDA path implements):
   log of sum(exp(scores)), sm_scale included.
 * attention_partial / lse_combine: the split-KV form of the same quantity,
   partial (o_i, lse_i) over a key range, merged by log-sum-exp weights.
+* accept_commit: each request advances by the tokens it accepted (same
+  section of the discuss.pytorch.kr article). Reading: block x_0..x_{T-1}
+  (x_0 = the target's previous output, x_1.. = drafts), target choices
+  y_0..y_{T-1}; draft x_{i+1} is accepted while it equals y_i; with a accepted
+  drafts the context grows by a + 1 and y_a is the next token.
 
 Everything is fp64 except the quantiser, whose fp32 roundings are part of the
 definition. Library primitives used as steps: numpy matmul, exp, log.
@@ -217,3 +222,29 @@ def lse_combine(partials):
     lse = m + np.log(np.sum(w, axis=0))
     o = sum(np.exp(l - lse)[..., None] * oi for oi, l in partials)
     return o, lse
+
+
+# ---------------------------------------------------------------------------
+# accept / commit
+# ---------------------------------------------------------------------------
+def accept_commit(block_tokens, target_tokens, block_lens, context_lens):
+    """Returns (accepted, new context_lens, next_tokens), one entry per sequence."""
+    accepted, new_ctx, nxt = [], [], []
+    off = 0
+    for b, T in enumerate(block_lens):
+        T = int(T)
+        x = list(block_tokens[off:off + T])
+        y = list(target_tokens[off:off + T])
+        off += T
+        if T == 0:
+            accepted.append(0)
+            new_ctx.append(int(context_lens[b]))
+            nxt.append(-1)
+            continue
+        a = 0
+        while a + 1 < T and x[a + 1] == y[a]:
+            a += 1
+        accepted.append(a)
+        new_ctx.append(int(context_lens[b]) + a + 1)
+        nxt.append(int(y[a]))
+    return (np.array(accepted, np.int32), np.array(new_ctx, np.int32), np.array(nxt, np.int32))

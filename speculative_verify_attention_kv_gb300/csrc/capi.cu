@@ -8,6 +8,11 @@ namespace splash {
 cudaError_t launch_kv_append(const float*, const float*, int, int8_t*, int8_t*, float*, float*,
                              const int32_t*, int, const int32_t*, const int32_t*, int, int, int,
                              int, int*, cudaStream_t);
+cudaError_t launch_kv_append_bf16(const __nv_bfloat16*, const __nv_bfloat16*, int, int8_t*,
+                                  int8_t*, float*, float*, const int32_t*, int, const int32_t*,
+                                  const int32_t*, int, int, int, int, int*, cudaStream_t);
+cudaError_t launch_accept_commit(const int32_t*, const int32_t*, int, const int32_t*, int32_t*,
+                                 int32_t*, int32_t*, int, int*, cudaStream_t);
 cudaError_t launch_plan(const int32_t*, const int32_t*, int, int, int, int, int, int, int, int,
                         int, int, int, int, unsigned char*, int*, cudaStream_t);
 cudaError_t launch_combine(int, int, int, int, int, int, int, const unsigned char*,
@@ -95,6 +100,43 @@ int splash_kv_append(const float* k_new, const float* v_new, int num_new_tokens,
                                    v_scales, page_table, max_pages_per_seq, context_lens,
                                    block_lens, num_seqs, num_kv_heads, head_dim, num_pages,
                                    device_status, stream);
+  return e == cudaSuccess ? SPLASH_OK : SPLASH_ERR_CUDA;
+}
+
+int splash_kv_append_bf16(const uint16_t* k_new, const uint16_t* v_new, int num_new_tokens,
+                          int8_t* k_pages, int8_t* v_pages, float* k_scales, float* v_scales,
+                          const int32_t* page_table, int max_pages_per_seq,
+                          const int32_t* context_lens, const int32_t* block_lens, int num_seqs,
+                          int num_kv_heads, int head_dim, int page_size, int num_pages,
+                          int* device_status, struct CUstream_st* stream) {
+  if (num_new_tokens < 0 || num_seqs < 0 || num_kv_heads <= 0 || num_pages < 0 ||
+      max_pages_per_seq <= 0)
+    return SPLASH_ERR_INVALID_ARGUMENT;
+  if (page_size != kPageSize || !head_dim_ok(head_dim)) return SPLASH_ERR_UNSUPPORTED;
+  if (num_new_tokens == 0 || num_seqs == 0) return SPLASH_OK;
+  if (!k_new || !v_new || !k_pages || !v_pages || !k_scales || !v_scales || !page_table ||
+      !context_lens || !block_lens)
+    return SPLASH_ERR_INVALID_ARGUMENT;
+  cudaError_t e = launch_kv_append_bf16(
+      reinterpret_cast<const __nv_bfloat16*>(k_new), reinterpret_cast<const __nv_bfloat16*>(v_new),
+      num_new_tokens, k_pages, v_pages, k_scales, v_scales, page_table, max_pages_per_seq,
+      context_lens, block_lens, num_seqs, num_kv_heads, head_dim, num_pages, device_status,
+      stream);
+  return e == cudaSuccess ? SPLASH_OK : SPLASH_ERR_CUDA;
+}
+
+int splash_accept_commit(const int32_t* block_tokens, const int32_t* target_tokens,
+                         int num_tokens, const int32_t* block_lens, int32_t* context_lens,
+                         int32_t* accepted, int32_t* next_tokens, int num_seqs,
+                         int* device_status, struct CUstream_st* stream) {
+  if (num_tokens < 0 || num_seqs < 0) return SPLASH_ERR_INVALID_ARGUMENT;
+  if (num_seqs == 0) return SPLASH_OK;
+  if (!block_lens || !context_lens || !accepted || !next_tokens ||
+      (num_tokens > 0 && (!block_tokens || !target_tokens)))
+    return SPLASH_ERR_INVALID_ARGUMENT;
+  cudaError_t e = launch_accept_commit(block_tokens, target_tokens, num_tokens, block_lens,
+                                       context_lens, accepted, next_tokens, num_seqs,
+                                       device_status, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SPLASH_OK : SPLASH_ERR_CUDA;
 }
 

@@ -1,17 +1,41 @@
 // kv_quantize_append: quantise a verify block's K/V rows to int8 and scatter
 // them into the paged cache.
 //
-// One warp per new token; the warp loops over the KV heads. A row of D fp32
-// values is spread over the 32 lanes (D/32 consecutive values per lane, 16-byte
-// loads), its absmax is a warp max, and each lane writes its D/32 codes as one
-// store. Scale and quotient use correctly rounded fp32 division (no fast-math
+// One warp per (new token, KV head) row; a CTA of 8 warps covers 8 / Hkv
+// tokens (one token when Hkv >= 8, its warps then loop over the heads). A row
+// of D fp32 values is spread over the 32 lanes (D/32 consecutive values per
+// lane, 16-byte loads), its absmax is a warp max, and each lane writes its D/32
+// codes as one store. Scale and quotient use correctly rounded fp32 division (no fast-math
 // in this translation unit), rounding is half-to-even (cvt.rni).
 #include "splash_common.cuh"
 
 namespace splash {
 
-constexpr int kAppendTokPerCta = 8;   // = warps per CTA
-constexpr int kAppendThreads = 32 * kAppendTokPerCta;
+constexpr int kAppendWarps = 8;
+constexpr int kAppendThreads = 32 * kAppendWarps;
+constexpr int kAppendTokPerCta = kAppendWarps;   // upper bound (Hkv = 1)
+
+template <int EPL>
+__device__ inline void load_row(const __nv_bfloat16* p, float (&x)[EPL]) {
+  // bf16 -> fp32 is exact
+  if constexpr (EPL == 2) {
+    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
+    x[0] = f.x; x[1] = f.y;
+  } else if constexpr (EPL == 4) {
+    const uint2 w = *reinterpret_cast<const uint2*>(p);
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w.x));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w.y));
+    x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y;
+  } else {
+    const uint4 w = *reinterpret_cast<const uint4*>(p);
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ws[i]));
+      x[2 * i] = f.x; x[2 * i + 1] = f.y;
+    }
+  }
+}
 
 template <int EPL>
 __device__ inline void load_row(const float* p, float (&x)[EPL]) {
@@ -55,21 +79,22 @@ __device__ inline void quantise_store(const float (&x)[EPL], int8_t* codes_dst, 
   if (lane == 0) *scale_dst = s;
 }
 
-template <int D>
+template <int D, typename TIn>
 __global__ void __launch_bounds__(kAppendThreads)
-kv_append_kernel(const float* __restrict__ k_new, const float* __restrict__ v_new,
+kv_append_kernel(const TIn* __restrict__ k_new, const TIn* __restrict__ v_new,
                  int num_new_tokens, int8_t* __restrict__ k_pages, int8_t* __restrict__ v_pages,
                  float* __restrict__ k_scales, float* __restrict__ v_scales,
                  const int32_t* __restrict__ page_table, int max_pages,
                  const int32_t* __restrict__ context_lens, const int32_t* __restrict__ block_lens,
-                 int num_seqs, int num_kv_heads, int num_pages, int* device_status) {
+                 int num_seqs, int num_kv_heads, int num_pages, int tok_per_cta,
+                 int* device_status) {
   constexpr int EPL = D / 32;
   __shared__ int s_seq[kAppendTokPerCta];
   __shared__ int s_first[kAppendTokPerCta];
   __shared__ int s_warp_tot[kAppendThreads / 32];
   __shared__ int s_running;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int tok0 = blockIdx.x * kAppendTokPerCta;
+  const int tok0 = blockIdx.x * tok_per_cta;
   if (tid < kAppendTokPerCta) s_seq[tid] = -1;
   if (tid == 0) s_running = 0;
   __syncthreads();
@@ -102,7 +127,7 @@ kv_append_kernel(const float* __restrict__ k_new, const float* __restrict__ v_ne
     }
     const int running = s_running;
     const int first = running + warp_off + incl - T;
-    const int lo = max(first, tok0), hi = min(first + T, tok0 + kAppendTokPerCta);
+    const int lo = max(first, tok0), hi = min(first + T, tok0 + tok_per_cta);
     for (int i = lo; i < hi; ++i) {
       s_seq[i - tok0] = b;
       s_first[i - tok0] = first;
@@ -110,45 +135,49 @@ kv_append_kernel(const float* __restrict__ k_new, const float* __restrict__ v_ne
     __syncthreads();
     if (tid == 0) s_running = running + chunk_tot;
     __syncthreads();
-    if (s_running >= tok0 + kAppendTokPerCta) break;
+    if (s_running >= tok0 + tok_per_cta) break;
   }
 
-  const int tok = tok0 + warp;
-  if (tok >= num_new_tokens) return;
-  const int b = s_seq[warp];
-  if (b < 0) return;  // row past sum(block_lens)
-  const int T = block_lens[b], ctx = context_lens[b];
-  if (T < 0 || ctx < 0 || (long long)ctx + T > (long long)max_pages * kPageSize) return;
-  const int pos = ctx + (tok - s_first[warp]);
-  const int page = page_table[(size_t)b * max_pages + pos / kPageSize];
-  if (page < 0 || page >= num_pages) {
-    if (lane == 0) report(device_status, SPLASH_DEVICE_BAD_PAGE);
-    return;
-  }
-  const int slot = pos % kPageSize;
-  for (int h = 0; h < num_kv_heads; ++h) {
+  for (int item = warp; item < tok_per_cta * num_kv_heads; item += kAppendWarps) {
+    const int ti = item / num_kv_heads, h = item % num_kv_heads;
+    const int tok = tok0 + ti;
+    if (tok >= num_new_tokens) break;
+    const int b = s_seq[ti];
+    if (b < 0) continue;  // row past sum(block_lens)
+    const int T = block_lens[b], ctx = context_lens[b];
+    if (T < 0 || ctx < 0 || (long long)ctx + T > (long long)max_pages * kPageSize) continue;
+    const int pos = ctx + (tok - s_first[ti]);
+    const int page = page_table[(size_t)b * max_pages + pos / kPageSize];
+    if (page < 0 || page >= num_pages) {
+      if (lane == 0) report(device_status, SPLASH_DEVICE_BAD_PAGE);
+      continue;
+    }
+    const int slot = pos % kPageSize;
     const size_t src = ((size_t)tok * num_kv_heads + h) * D + lane * EPL;
     const size_t row = ((size_t)page * num_kv_heads + h) * kPageSize + slot;
-    float x[EPL];
-    load_row<EPL>(k_new + src, x);
-    quantise_store<EPL>(x, k_pages + row * D + lane * EPL, k_scales + row, lane);
-    load_row<EPL>(v_new + src, x);
-    quantise_store<EPL>(x, v_pages + row * D + lane * EPL, v_scales + row, lane);
+    float xk[EPL], xv[EPL];
+    load_row<EPL>(k_new + src, xk);
+    load_row<EPL>(v_new + src, xv);
+    quantise_store<EPL>(xk, k_pages + row * D + lane * EPL, k_scales + row, lane);
+    quantise_store<EPL>(xv, v_pages + row * D + lane * EPL, v_scales + row, lane);
   }
 }
 
-cudaError_t launch_kv_append(const float* k_new, const float* v_new, int num_new_tokens,
-                             int8_t* k_pages, int8_t* v_pages, float* k_scales, float* v_scales,
-                             const int32_t* page_table, int max_pages,
-                             const int32_t* context_lens, const int32_t* block_lens, int num_seqs,
-                             int num_kv_heads, int head_dim, int num_pages, int* device_status,
-                             cudaStream_t stream) {
+template <typename TIn>
+cudaError_t launch_kv_append_t(const TIn* k_new, const TIn* v_new, int num_new_tokens,
+                               int8_t* k_pages, int8_t* v_pages, float* k_scales, float* v_scales,
+                               const int32_t* page_table, int max_pages,
+                               const int32_t* context_lens, const int32_t* block_lens,
+                               int num_seqs, int num_kv_heads, int head_dim, int num_pages,
+                               int* device_status, cudaStream_t stream) {
   if (num_new_tokens == 0 || num_seqs == 0) return cudaSuccess;
-  const int grid = (num_new_tokens + kAppendTokPerCta - 1) / kAppendTokPerCta;
+  const int tok_per_cta = num_kv_heads >= kAppendWarps ? 1 : kAppendWarps / num_kv_heads;
+  const int grid = (num_new_tokens + tok_per_cta - 1) / tok_per_cta;
 #define SPLASH_APPEND(DD)                                                                   \
-  kv_append_kernel<DD><<<grid, kAppendThreads, 0, stream>>>(                                \
+  kv_append_kernel<DD, TIn><<<grid, kAppendThreads, 0, stream>>>(                                \
       k_new, v_new, num_new_tokens, k_pages, v_pages, k_scales, v_scales, page_table,       \
-      max_pages, context_lens, block_lens, num_seqs, num_kv_heads, num_pages, device_status)
+      max_pages, context_lens, block_lens, num_seqs, num_kv_heads, num_pages, tok_per_cta,   \
+      device_status)
   switch (head_dim) {
     case 64: SPLASH_APPEND(64); break;
     case 128: SPLASH_APPEND(128); break;
@@ -157,6 +186,31 @@ cudaError_t launch_kv_append(const float* k_new, const float* v_new, int num_new
   }
 #undef SPLASH_APPEND
   return cudaGetLastError();
+}
+
+cudaError_t launch_kv_append(const float* k_new, const float* v_new, int num_new_tokens,
+                             int8_t* k_pages, int8_t* v_pages, float* k_scales, float* v_scales,
+                             const int32_t* page_table, int max_pages,
+                             const int32_t* context_lens, const int32_t* block_lens, int num_seqs,
+                             int num_kv_heads, int head_dim, int num_pages, int* device_status,
+                             cudaStream_t stream) {
+  return launch_kv_append_t<float>(k_new, v_new, num_new_tokens, k_pages, v_pages, k_scales,
+                                   v_scales, page_table, max_pages, context_lens, block_lens,
+                                   num_seqs, num_kv_heads, head_dim, num_pages, device_status,
+                                   stream);
+}
+
+cudaError_t launch_kv_append_bf16(const __nv_bfloat16* k_new, const __nv_bfloat16* v_new,
+                                  int num_new_tokens, int8_t* k_pages, int8_t* v_pages,
+                                  float* k_scales, float* v_scales, const int32_t* page_table,
+                                  int max_pages, const int32_t* context_lens,
+                                  const int32_t* block_lens, int num_seqs, int num_kv_heads,
+                                  int head_dim, int num_pages, int* device_status,
+                                  cudaStream_t stream) {
+  return launch_kv_append_t<__nv_bfloat16>(k_new, v_new, num_new_tokens, k_pages, v_pages,
+                                           k_scales, v_scales, page_table, max_pages,
+                                           context_lens, block_lens, num_seqs, num_kv_heads,
+                                           head_dim, num_pages, device_status, stream);
 }
 
 }  // namespace splash

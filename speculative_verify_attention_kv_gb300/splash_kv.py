@@ -41,6 +41,10 @@ def _load() -> ctypes.CDLL:
     lib.splash_tensor_path_supported.argtypes = [I]
     lib.splash_kv_append.restype = I
     lib.splash_kv_append.argtypes = [P, P, I, P, P, P, P, P, I, P, P, I, I, I, I, I, P, P]
+    lib.splash_kv_append_bf16.restype = I
+    lib.splash_kv_append_bf16.argtypes = [P, P, I, P, P, P, P, P, I, P, P, I, I, I, I, I, P, P]
+    lib.splash_accept_commit.restype = I
+    lib.splash_accept_commit.argtypes = [P, P, I, P, P, P, P, I, P, P]
     lib.splash_verify_attention_workspace_size.restype = S
     lib.splash_verify_attention_workspace_size.argtypes = [I, I, I, I, I, I]
     attn = [P, I, P, P, P, P, P, I, P, P, I, I, I, I, I, I, I, F, P, P, P, S, P, P]
@@ -59,7 +63,7 @@ def _load() -> ctypes.CDLL:
 
 LIB = _load()
 EXPORTED = ("splash_status_string", "splash_abi_version", "splash_tensor_path_supported",
-            "splash_kv_append",
+            "splash_kv_append", "splash_kv_append_bf16", "splash_accept_commit",
             "splash_verify_attention_workspace_size", "splash_verify_attention",
             "splash_verify_attention_tuned", "splash_verify_attention_profiled",
             "splash_verify_attention_fixed_scratch_bytes", "splash_verify_attention_fixed_scratch")
@@ -107,8 +111,11 @@ def alloc_pool(num_pages: int, num_kv_heads: int, head_dim: int, device="cuda"):
 
 def splash_kv_append(k_new, v_new, k_pages, v_pages, k_scales, v_scales, page_table,
                      context_lens, block_lens, device_status=None, stream=None) -> None:
-    _check(k_new, "k_new", torch.float32, 3)
-    _check(v_new, "v_new", torch.float32, 3)
+    """k_new / v_new: float32 (splash_kv_append) or bfloat16 (splash_kv_append_bf16)."""
+    if k_new.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("k_new must be float32 or bfloat16")
+    _check(k_new, "k_new", k_new.dtype, 3)
+    _check(v_new, "v_new", k_new.dtype, 3)
     for n, t in (("k_pages", k_pages), ("v_pages", v_pages)):
         _check(t, n, torch.int8, 4)
     for n, t in (("k_scales", k_scales), ("v_scales", v_scales)):
@@ -122,13 +129,34 @@ def splash_kv_append(k_new, v_new, k_pages, v_pages, k_scales, v_scales, page_ta
     if tuple(v_pages.shape) != (num_pages, hkv, P, D) or tuple(k_new.shape[1:]) != (hkv, D) \
             or k_new.shape != v_new.shape:
         raise ValueError("shape mismatch between k_new/v_new and the pool")
-    st = LIB.splash_kv_append(
+    fn = LIB.splash_kv_append if k_new.dtype == torch.float32 else LIB.splash_kv_append_bf16
+    st = fn(
         _ptr(k_new), _ptr(v_new), k_new.shape[0], _ptr(k_pages), _ptr(v_pages), _ptr(k_scales),
         _ptr(v_scales), _ptr(page_table), page_table.shape[1], _ptr(context_lens),
         _ptr(block_lens), context_lens.shape[0], hkv, D, P, num_pages, _ptr(device_status),
         _stream(stream))
     if st != 0:
         raise SplashError(st, "splash_kv_append")
+
+
+def splash_accept_commit(block_tokens, target_tokens, block_lens, context_lens, accepted,
+                         next_tokens, device_status=None, stream=None) -> None:
+    """Advance context_lens (in place) by the accepted drafts plus one."""
+    for n, t in (("block_tokens", block_tokens), ("target_tokens", target_tokens),
+                 ("block_lens", block_lens), ("context_lens", context_lens),
+                 ("accepted", accepted), ("next_tokens", next_tokens)):
+        _check(t, n, torch.int32, 1)
+    if device_status is not None:
+        _check(device_status, "device_status", torch.int32)
+    B = block_lens.shape[0]
+    if context_lens.shape[0] != B or accepted.shape[0] != B or next_tokens.shape[0] != B \
+            or target_tokens.shape != block_tokens.shape:
+        raise ValueError("shape mismatch")
+    st = LIB.splash_accept_commit(_ptr(block_tokens), _ptr(target_tokens), block_tokens.shape[0],
+                                  _ptr(block_lens), _ptr(context_lens), _ptr(accepted),
+                                  _ptr(next_tokens), B, _ptr(device_status), _stream(stream))
+    if st != 0:
+        raise SplashError(st, "splash_accept_commit")
 
 
 def splash_verify_attention_workspace_size(num_seqs: int, num_q_tokens: int, num_q_heads: int,

@@ -6,6 +6,7 @@ Bars: int8 codes and fp32 scales bit-exact; attention O (bf16) within max-abs
 from __future__ import annotations
 
 import functools
+import json
 
 import numpy as np
 import pytest
@@ -99,6 +100,73 @@ def test_kv_append_bit_exact_edge_rows(D):
     assert np.array_equal(kp, opool.k_codes) and np.array_equal(vp, opool.v_codes)
     assert np.array_equal(ks.view(np.uint32), opool.k_scales.view(np.uint32))
     assert np.array_equal(vs.view(np.uint32), opool.v_scales.view(np.uint32))
+
+
+@pytest.mark.parametrize("D", [128, 256])
+def test_kv_append_bf16_bit_exact(D):
+    rng = np.random.default_rng(100 + D)
+    n, hkv = 53, 4
+    x = rng.standard_normal((n, hkv, D)).astype(np.float32) * np.float32(3.0)
+    x[0, 1, :] = 0
+    x[1, 2, :] = 0
+    x[1, 2, 9] = np.float32(2.0 ** -133)         # a bf16 subnormal
+    x[2] *= np.float32(1e20)
+    xb = wl.bf16_bits_from_f32(x)
+    vb = wl.bf16_bits_from_f32(-0.5 * x)
+    W = wl.custom(2 * hkv, hkv, D, [5, 0, 33], [20, 1, n - 21], seed=4)
+    pool = sk.alloc_pool(W.num_pages, hkv, D)
+    table = torch.from_numpy(W.page_table).cuda()
+    as_bf16 = lambda b: torch.from_numpy(b.view(np.int16)).cuda().view(torch.bfloat16)
+    sk.splash_kv_append(as_bf16(xb), as_bf16(vb), *pool, table,
+                        torch.from_numpy(W.context_lens).cuda(), torch.from_numpy(W.block_lens).cuda())
+    torch.cuda.synchronize()
+    opool = O.PagedPool(W.num_pages, hkv, 16, D)
+    O.kv_append(opool, wl.f32_from_bf16_bits(xb), wl.f32_from_bf16_bits(vb), W.page_table,
+                W.context_lens, W.block_lens)
+    kp, vp, ks, vs = [t.cpu().numpy() for t in pool]
+    assert np.array_equal(kp, opool.k_codes) and np.array_equal(vp, opool.v_codes)
+    assert np.array_equal(ks.view(np.uint32), opool.k_scales.view(np.uint32))
+    assert np.array_equal(vs.view(np.uint32), opool.v_scales.view(np.uint32))
+
+
+# ---------------------------------------------------------------------------
+# accept / commit: exact integers
+# ---------------------------------------------------------------------------
+def _accept_on_gpu(x, y, T, ctx):
+    i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.int32)).cuda()
+    ctx_d = i32(ctx)
+    acc = torch.full((len(T),), -7, dtype=torch.int32, device="cuda")
+    nxt = torch.full((len(T),), -7, dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    sk.splash_accept_commit(i32(x), i32(y), i32(T), ctx_d, acc, nxt, device_status=status)
+    torch.cuda.synchronize()
+    return acc.cpu().numpy(), ctx_d.cpu().numpy(), nxt.cpu().numpy(), int(status.item())
+
+
+def test_accept_commit_golden_cases():
+    with open(os.path.join(os.path.dirname(__file__), "golden", "accept_commit_cases.json")) as f:
+        c = json.load(f)
+    acc, ctx, nxt, st = _accept_on_gpu(c["block_tokens"], c["target_tokens"], c["block_lens"],
+                                       c["context_lens"])
+    assert st == 0
+    assert acc.tolist() == c["accepted"]
+    assert ctx.tolist() == c["new_context"]
+    assert nxt.tolist() == c["next_tokens"]
+
+
+@pytest.mark.parametrize("B", [1, 64, 1000, 5000])
+def test_accept_commit_random_matches_oracle(B):
+    rng = np.random.default_rng(B)
+    T = rng.integers(0, 17, size=B)
+    T[rng.random(B) < 0.1] = 0
+    n = int(T.sum())
+    x = rng.integers(0, 3, size=n)            # a small vocabulary makes long accepted runs
+    y = rng.integers(0, 3, size=n)
+    ctx = rng.integers(0, 40000, size=B)
+    acc, new_ctx, nxt, st = _accept_on_gpu(x, y, T, ctx)
+    ra, rc, rn = O.accept_commit(x, y, T, ctx)
+    assert st == 0
+    assert np.array_equal(acc, ra) and np.array_equal(new_ctx, rc) and np.array_equal(nxt, rn)
 
 
 # ---------------------------------------------------------------------------

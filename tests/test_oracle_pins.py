@@ -376,3 +376,33 @@ def test_planted_combine_mistake_is_caught(monkeypatch):
         return o, lse
     monkeypatch.setattr(O, "lse_combine", bad_combine)
     assert _pins_fail(lambda: test_split_kv_equals_unsplit([0, 16, 32, 53]))
+
+
+# ---------------------------------------------------------------------------
+# accept / commit
+# ---------------------------------------------------------------------------
+def test_accept_commit_hand_cases():
+    with open(os.path.join(GOLDEN, "accept_commit_cases.json")) as f:
+        c = json.load(f)
+    acc, ctx, nxt = O.accept_commit(c["block_tokens"], c["target_tokens"], c["block_lens"],
+                                    c["context_lens"])
+    assert acc.tolist() == c["accepted"]
+    assert ctx.tolist() == c["new_context"]
+    assert nxt.tolist() == c["next_tokens"]
+
+
+def test_accept_commit_bounds_and_full_acceptance():
+    rng = np.random.default_rng(3)
+    T = rng.integers(0, 17, size=50)
+    x = rng.integers(0, 5, size=int(T.sum()))
+    y = rng.integers(0, 5, size=int(T.sum()))
+    acc, ctx, nxt = O.accept_commit(x, y, T, np.zeros(50, np.int32))
+    assert np.all((acc >= 0) & (acc <= np.maximum(T - 1, 0)))
+    assert np.array_equal(ctx, np.where(T > 0, acc + 1, 0))
+    # target agrees with every draft -> all T-1 drafts accepted
+    y2 = np.concatenate([np.append(x[o + 1:o + t], 99) for o, t in
+                         zip(np.concatenate([[0], np.cumsum(T)[:-1]]), T) if t > 0])
+    x2 = np.concatenate([x[o:o + t] for o, t in zip(np.concatenate([[0], np.cumsum(T)[:-1]]), T) if t > 0])
+    acc2, _, nxt2 = O.accept_commit(x2, y2, T, np.zeros(50, np.int32))
+    assert np.array_equal(acc2, np.maximum(T - 1, 0))
+    assert np.all(nxt2[T > 0] == 99)
