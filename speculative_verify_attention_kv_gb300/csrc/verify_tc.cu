@@ -21,11 +21,13 @@
 //               over 4 threads (2 rows per thread, row reductions = 2 shuffles)
 //   warps 8-11  converters: int8 codes from the staging ring -> fp16 in
 //               registers -> 128B-swizzled SMEM tiles (K: K-major, V: MN-major)
-//   warp  12    TMEM allocation; one thread issues the QK MMAs
-//   warp  13    one thread issues the PV MMAs (two issuing threads keep the
-//               tensor pipe fed better than one)
-//   warps 14-15 producers, one per staging-ring stage (even / odd tiles):
-//               bulk async copies (TMA, untiled) of whole
+//   warp  12    TMEM allocation; one thread issues the QK MMAs of even tiles
+//   warp  13    one thread issues the QK MMAs of odd tiles
+//   warp  14    one thread issues the PV MMAs
+//               (one thread issues at most one tcgen05.mma per ~120 cycles
+//               whatever N is; with A in TMEM, three issuing threads give
+//               nearly three times the rate of one)
+//   warp  15    producer: bulk async copies (TMA, untiled) of whole
 //               (page, KV head) blocks: codes into a 2-stage int8 staging
 //               ring ahead of the converters, scales straight into the
 //               3-stage scale arrays the softmax reads
@@ -46,10 +48,14 @@ constexpr int kRing = 2;                      // int8 staging stages
 constexpr int kSoftmaxWarps = 8;              // 2 per TMEM lane quarter, 16 rows each
 constexpr int kLoadWarps = 4;
 constexpr int kLoadThreads = 32 * kLoadWarps;
-constexpr int kMmaWarp = kSoftmaxWarps + kLoadWarps;   // TMEM allocation, QK issue
-constexpr int kPvWarp = kMmaWarp + 1;                   // PV issue
-constexpr int kProducerWarp = kPvWarp + 1;              // first of kRing producer warps
-constexpr int kThreads = 32 * (kProducerWarp + kRing);
+constexpr int kMmaWarp = kSoftmaxWarps + kLoadWarps;   // TMEM allocation, QK issue (even tiles)
+constexpr int kQkOddWarp = kMmaWarp + 1;                // QK issue (odd tiles)
+constexpr int kPvWarp = kQkOddWarp + 1;                 // PV issue
+constexpr int kProducerWarp = kPvWarp + 1;
+// 16 warps = 4 per SM sub-partition, so each thread may hold 128 registers
+constexpr int kThreads = 32 * (kProducerWarp + 1);
+static_assert(kThreads == 512, "warp roles");
+static_assert(kStages == 2, "one QK-issuing warp per S/P buffer");
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.0f;          // lazy rescale threshold (factor 256)
 constexpr unsigned long long kWaitNs = 1000000000ull;
@@ -301,8 +307,10 @@ struct Smem {
   uint64_t p_full[kStages];       // softmax -> MMA
   uint64_t p_free[kStages];       // PV of the buffer's tile done -> MMA (QK may
                                   // overwrite the S/P buffer), softmax (O rescale, epilogue)
-  uint64_t q_full;                // softmax (Q' in TMEM) -> MMA
-  uint64_t drain[2];              // QK / PV issuer: all of its MMAs complete
+  uint64_t q_full;                // softmax (Q' in TMEM) -> QK issuers
+  uint64_t q_ack;                 // both QK issuers saw q_full -> softmax (the next
+                                  // segment's Q' may complete q_full's next phase)
+  uint64_t drain[3];              // QK even / QK odd / PV issuer: its MMAs complete
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -490,8 +498,8 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
       mbar_init(smem_u32(&sh->v_free[s]), 1);
     }
     mbar_init(smem_u32(&sh->q_full), 32 * kSoftmaxWarps);
-    mbar_init(smem_u32(&sh->drain[0]), 1);
-    mbar_init(smem_u32(&sh->drain[1]), 1);
+    mbar_init(smem_u32(&sh->q_ack), 2);
+    for (int i = 0; i < 3; ++i) mbar_init(smem_u32(&sh->drain[i]), 1);
     sh->abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -515,10 +523,17 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
     const uint32_t lane_base = (uint32_t)lb << 16;
     const int quad = lane & 3;                            // column pair within 8 columns
     const int rr[2] = {lb + (lane >> 2), lb + 8 + (lane >> 2)};
-    int g = 0;
+    int g = 0, nsegs = 0;
     Seg s;
     bool ok = true;
     while (ok && iter.next(s)) {
+      // Q' of this segment overwrites the previous one: both QK issuers must
+      // have seen the previous q_full phase (so neither lags it by two phases)
+      if (nsegs > 0) {
+        ok = sync.wait(smem_u32(&sh->q_ack), (nsegs - 1) & 1);
+        if (!ok) break;
+      }
+      ++nsegs;
       const bool warp_live = lb < s.R;
       bool live[2];
       int lim[2];
@@ -652,7 +667,6 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
             m[k] = m_use;
             base[k] = (m_use == -INFINITY) ? 0.f : rowfac[k] * m_use;
           }
-#pragma unroll
           float2 vs2[8];
 #pragma unroll
           for (int i4 = 0; i4 < 4; ++i4) {
@@ -660,6 +674,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
             vs2[2 * i4] = make_float2(vq4.x, vq4.y);
             vs2[2 * i4 + 1] = make_float2(vq4.z, vq4.w);
           }
+#pragma unroll
           for (int k = 0; k < 2; ++k) {
             const float2 rf2 = make_float2(rowfac[k], rowfac[k]);
             const float2 nb2 = make_float2(-base[k], -base[k]);
@@ -789,9 +804,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
       }
     }
   } else if (warp >= kProducerWarp) {
-    // =========================================================== producers
-    // producer warp `mine` stages the tiles of ring stage `mine` (g % kRing)
-    const int mine = warp - kProducerWarp;
+    // ============================================================ producer
     int g = 0;
     Seg s;
     bool ok = true;
@@ -799,7 +812,6 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
     while (ok && iter.next(s)) {
       for (int it = s.i0; it < s.i1; ++it, ++g) {
         const int r = g % kRing, vst = g % kVStages;
-        if (r != mine) continue;
         if (lane == 0) {
           // ring stage free (converted), scale stage free (read by the softmax
           // of the tile three back)
@@ -814,11 +826,14 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
     }
   } else {
     // ============================================================ MMA issue
-    // warp kMmaWarp: QK(i) into S[i % 2] once its K tile is converted and the
-    // PV that last read that S/P buffer (tile i - 2) has completed (issue order
-    // alone does not order a later TMEM write after an earlier MMA's read).
+    // warps kMmaWarp / kQkOddWarp: QK(i) (i even / odd) into S[i % 2] once its
+    // K tile is converted and the PV that last read that S/P buffer (tile
+    // i - 2) has completed (issue order alone does not order a later TMEM
+    // write after an earlier MMA's read).
     // warp kPvWarp: PV(i) into O once the softmax has written P(i).
-    const bool is_qk = warp == kMmaWarp;
+    const bool is_qk = warp != kPvWarp;
+    const int qk_par = warp - kMmaWarp;          // tiles of this parity (QK issuers)
+    const int role = is_qk ? qk_par : 2;
     if (lane == 0) {
       constexpr uint32_t kIdescQK = idesc_f16(128, kTileKeys, 0);
       constexpr uint32_t kIdescPV = idesc_f16(128, D, 1);
@@ -833,10 +848,12 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
           ok = sync.wait(smem_u32(&sh->q_full), nsegs & 1);
           if (!ok) break;
           fence_after();
+          mbar_arrive(smem_u32(&sh->q_ack));
         }
         for (int it = s.i0; it < s.i1 && ok; ++it, ++g) {
           const int st = g % kStages, vst = g % kVStages;
           if (is_qk) {
+            if (st != qk_par) continue;
             ok = sync.wait(smem_u32(&sh->p_free[st]), ((g / kStages) & 1) ^ 1) &&
                  sync.wait(smem_u32(&sh->kv_full[st]), (g / kStages) & 1);
             if (!ok) break;
@@ -865,8 +882,8 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
         ++nsegs;
       }
       // every MMA this thread issued is complete before TMEM is released
-      mma_commit(smem_u32(&sh->drain[is_qk ? 0 : 1]));
-      sync.wait(smem_u32(&sh->drain[is_qk ? 0 : 1]), 0);
+      mma_commit(smem_u32(&sh->drain[role]));
+      sync.wait(smem_u32(&sh->drain[role]), 0);
     }
     __syncwarp();
   }
