@@ -296,11 +296,12 @@ struct SegIter {
 };
 
 struct Smem {
-  uint64_t ring_full[kRing];      // producer tx -> converters
-  uint64_t ring_empty[kRing];     // converters -> producer
+  uint64_t ring_full[2][kRing];   // producer tx -> converters ([0] K codes, [1] V codes)
+  uint64_t ring_empty[2][kRing];  // converters -> producer
   uint64_t sc_full[kVStages];     // producer cp.async (scales) -> softmax
   uint64_t sc_free[kVStages];     // softmax done with the scales -> producer
-  uint64_t kv_full[kStages];      // converters -> MMA (fp16 K and V of the tile ready)
+  uint64_t k_full[kStages];       // converters -> QK issuer (fp16 K of the tile ready)
+  uint64_t v_full[kVStages];      // converters -> PV issuer (fp16 V of the tile ready)
   uint64_t k_free[kStages];       // QK done -> converters
   uint64_t v_free[kVStages];      // PV done -> converters, producer (scales)
   uint64_t s_full[kStages];       // QK done -> softmax
@@ -360,47 +361,38 @@ struct PageWindow {
   }
 };
 
-// Producer (one warp): stage tile `it` of segment s. The tile's 4 page ids
-// come from the page window; lanes 0..7 issue one bulk copy each (K or V codes
-// of one page into the ring stage); every lane moves 16 bytes of scales into
-// the scale arrays with cp.async. Pages past the sequence end or with an invalid id are
-// skipped: their stale codes are finite and the softmax gives their keys
-// probability 0 without reading their scales.
+// Producer (one warp): the K or the V codes of tile `it` of segment s into a
+// ring entry. The tile's 4 page ids come from the page window; lanes 0..3
+// each issue one bulk copy (the codes of one (page, KV head) block). Pages
+// past the sequence end or with an invalid id are skipped: their stale codes
+// are finite and the softmax gives their keys probability 0 without reading
+// their scales. Returns the page id of page (lane & 3), -1 if skipped.
 template <int D>
-__device__ __forceinline__ void stage_tile(const AttnParams& p, const Seg& s, int it,
-                                           uint8_t* stage, float* scales, uint32_t ring_bar,
-                                           uint32_t scale_bar, int lane, PageWindow& win) {
-  using C = Cfg<D>;
+__device__ __forceinline__ int stage_codes(const AttnParams& p, const Seg& s, int it,
+                                           const int8_t* pool, uint8_t* dst, uint32_t bar,
+                                           int lane, PageWindow& win) {
   const int k0 = it * kTileKeys;
   const int npages = (s.Lk + kPageSize - 1) / kPageSize;
-  // every lane holds the id of page (lane & 3) of this tile
   int page = win.get(p, s.b, k0 / kPageSize, npages, lane);
-  const int j = lane & 3;
-  if (k0 + kPageSize * j >= s.Lk) page = -1;
-  if (page >= p.num_pages) page = -1;
-  const bool bad = (k0 + kPageSize * j < s.Lk) && page < 0;
-  if (bad && lane < kPagesPerTile) report(p.device_status, SPLASH_DEVICE_BAD_PAGE);
+  const bool needed = k0 + kPageSize * (lane & 3) < s.Lk;
+  if (!needed || page >= p.num_pages) page = -1;
+  if (needed && page < 0 && lane < kPagesPerTile) report(p.device_status, SPLASH_DEVICE_BAD_PAGE);
   const int mask = (int)(__ballot_sync(0xffffffffu, page >= 0 && lane < kPagesPerTile) &
                          ((1u << kPagesPerTile) - 1));
   constexpr uint32_t kBlock = kPageSize * D;          // codes of one (page, head)
-  if (lane == 0) mbar_expect_tx(ring_bar, (uint32_t)__popc(mask) * (2 * kBlock));
+  if (lane == 0) mbar_expect_tx(bar, (uint32_t)__popc(mask) * kBlock);
   __syncwarp();
-  // codes: one bulk copy per (page, tensor), lanes 0..7
-  if (lane < 2 * kPagesPerTile) {
-    const int pj = __shfl_sync(0x000000ffu, page, lane >> 1);
-    if (pj >= 0) {
-      const size_t blk = (size_t)pj * p.num_kv_heads + s.h;
-      const int jj = lane >> 1;
-      if ((lane & 1) == 0)
-        bulk_g2s(smem_u32(stage) + jj * kBlock, p.k_pages + blk * kBlock, kBlock, ring_bar);
-      else
-        bulk_g2s(smem_u32(stage) + C::kRingCodes + jj * kBlock, p.v_pages + blk * kBlock,
-                 kBlock, ring_bar);
-    }
-  }
-  // scales: 16 bytes per lane by cp.async (lanes 0..15 K, 16..31 V; page
-  // (lane & 15) / 4, slots 4 * (lane & 3) ..); each lane's arrival on the
-  // scale barrier fires when its copy has landed
+  if (lane < kPagesPerTile && page >= 0)
+    bulk_g2s(smem_u32(dst) + lane * kBlock,
+             pool + ((size_t)page * p.num_kv_heads + s.h) * kBlock, kBlock, bar);
+  return page;
+}
+
+// Producer: the tile's K and V scales, 16 bytes per lane by cp.async (lanes
+// 0..15 K, 16..31 V; page (lane & 15) / 4, slots 4 * (lane & 3) ..); each
+// lane's arrival on the scale barrier fires when its copy has landed.
+__device__ __forceinline__ void stage_scales(const AttnParams& p, const Seg& s, int page,
+                                             float* scales, uint32_t scale_bar, int lane) {
   const int sj = (lane & 15) >> 2;
   const int ps = __shfl_sync(0xffffffffu, page, sj);
   if (ps >= 0) {
@@ -424,23 +416,29 @@ __host__ __device__ constexpr int tile_row_of_key(int n) {
 
 template <int D>
 __device__ __forceinline__ void convert_codes(const uint8_t* src, uint8_t* dst, int lt) {
-  constexpr int kUnits = kTileKeys * D / 8;
+  // units of 16 codes (one 16-byte load, two 16-byte fp16 stores); a warp
+  // covers two key rows, and the 128B swizzle keeps its stores conflict-free
+  constexpr int kUnits = kTileKeys * D / 16;
   constexpr int kPer = kUnits / kLoadThreads;
-  uint2 w[kPer];
+  static_assert(kUnits % kLoadThreads == 0, "converter units");
+  uint4 w[kPer];
 #pragma unroll
   for (int q = 0; q < kPer; ++q) {
     const int u = q * kLoadThreads + lt;
-    w[q] = *reinterpret_cast<const uint2*>(src + (u / (D / 8)) * D + (u % (D / 8)) * 8);
+    w[q] = *reinterpret_cast<const uint4*>(src + (u / (D / 16)) * D + (u % (D / 16)) * 16);
   }
 #pragma unroll
   for (int q = 0; q < kPer; ++q) {
     const int u = q * kLoadThreads + lt;
-    const int n = tile_row_of_key(u / (D / 8)), c8 = u % (D / 8);
-    uint4 h;
-    i8x4_to_h2x2(w[q].x, h.x, h.y);
-    i8x4_to_h2x2(w[q].y, h.z, h.w);
-    const uint32_t a = (c8 / 8) * (kTileKeys * 128) + n * 128 + (((c8 & 7) ^ (n & 7)) << 4);
-    *reinterpret_cast<uint4*>(dst + a) = h;
+    const int n = tile_row_of_key(u / (D / 16)), c8 = 2 * (u % (D / 16));
+    uint4 h0, h1;
+    i8x4_to_h2x2(w[q].x, h0.x, h0.y);
+    i8x4_to_h2x2(w[q].y, h0.z, h0.w);
+    i8x4_to_h2x2(w[q].z, h1.x, h1.y);
+    i8x4_to_h2x2(w[q].w, h1.z, h1.w);
+    const uint32_t row = (c8 / 8) * (kTileKeys * 128) + n * 128;
+    *reinterpret_cast<uint4*>(dst + row + (((c8 & 7) ^ (n & 7)) << 4)) = h0;
+    *reinterpret_cast<uint4*>(dst + row + ((((c8 + 1) & 7) ^ (n & 7)) << 4)) = h1;
   }
 }
 
@@ -481,12 +479,13 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
   float* lse_part = reinterpret_cast<float*>(p.ws + L.lse_part);
 
   if (tid == 0) {
-    for (int s = 0; s < kRing; ++s) {
-      mbar_init(smem_u32(&sh->ring_full[s]), 1);
-      mbar_init(smem_u32(&sh->ring_empty[s]), kLoadThreads);
-    }
+    for (int s = 0; s < kRing; ++s)
+      for (int kv = 0; kv < 2; ++kv) {
+        mbar_init(smem_u32(&sh->ring_full[kv][s]), 1);
+        mbar_init(smem_u32(&sh->ring_empty[kv][s]), kLoadThreads);
+      }
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(smem_u32(&sh->kv_full[s]), kLoadThreads);
+      mbar_init(smem_u32(&sh->k_full[s]), kLoadThreads);
       mbar_init(smem_u32(&sh->k_free[s]), 1);
       mbar_init(smem_u32(&sh->s_full[s]), 1);
       mbar_init(smem_u32(&sh->p_full[s]), 32 * kSoftmaxWarps);
@@ -496,6 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
       mbar_init(smem_u32(&sh->sc_full[s]), 32);     // one cp.async arrival per producer lane
       mbar_init(smem_u32(&sh->sc_free[s]), 32 * kSoftmaxWarps);
       mbar_init(smem_u32(&sh->v_free[s]), 1);
+      mbar_init(smem_u32(&sh->v_full[s]), kLoadThreads);
     }
     mbar_init(smem_u32(&sh->q_full), 32 * kSoftmaxWarps);
     mbar_init(smem_u32(&sh->q_ack), 2);
@@ -547,21 +547,27 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
       }
       float rowfac[2] = {0.f, 0.f};
       // Q rows -> TMEM as fp16 after an exact per-row power-of-two rescale.
-      // Thread covers d = 8i + 2*quad + {0,1} (i < D/8) of both rows.
+      // Thread covers d = 8i + 2*quad + {0,1} (i < D/8) of both rows; all of
+      // its Q words are loaded in one batch (one memory latency per segment).
       if (warp_live) {
+        uint32_t qw[2][D / 8];                             // bf16 pairs
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const uint32_t* qr = reinterpret_cast<const uint32_t*>(p.q + qrow_off[k] * D) + quad;
+#pragma unroll
+          for (int i = 0; i < D / 8; ++i) {
+            qw[k][i] = 0u;
+            if (live[k]) qw[k][i] = __ldg(qr + 4 * i);
+          }
+        }
         float up[2];
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
-          float amax = 0.f;
-          if (live[k]) {
-            const __nv_bfloat162* qr =
-                reinterpret_cast<const __nv_bfloat162*>(p.q + qrow_off[k] * D) + quad;
-#pragma unroll 8
-            for (int i = 0; i < D / 8; ++i) {
-              const float2 f = __bfloat1622float2(qr[4 * i]);
-              amax = fmax3(amax, fabsf(f.x), fabsf(f.y));
-            }
-          }
+          uint32_t amax_bits = 0;                          // max |q| as bf16 magnitude bits
+#pragma unroll
+          for (int i = 0; i < D / 8; ++i)
+            amax_bits = max(amax_bits, max(qw[k][i] & 0x7fffu, (qw[k][i] >> 16) & 0x7fffu));
+          float amax = __uint_as_float(amax_bits << 16);
           amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
           amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
           // 2^e with max|q| * 2^e in [2^14, 2^15)
@@ -572,20 +578,19 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
           up[k] = __uint_as_float((uint32_t)(e + 127) << 23);
           rowfac[k] = p.sm_scale_log2 / up[k];
         }
-#pragma unroll 1
+#pragma unroll
         for (int c0 = 0; c0 < D / 2; c0 += 64) {          // 64 packed columns per pass
 #pragma unroll
           for (int half = 0; half < 2; ++half) {
             uint32_t v[32];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-              const int col = c0 + 32 * half + 4 * i + quad;     // packed column = d pair
+              // packed column c0 + 32*half + 4i + quad holds d pair 8j + 2*quad
+              const int j = (c0 + 32 * half) / 4 + i;
 #pragma unroll
               for (int k = 0; k < 2; ++k) {
-                float2 f = make_float2(0.f, 0.f);
-                if (live[k])
-                  f = __bfloat1622float2(
-                      reinterpret_cast<const __nv_bfloat162*>(p.q + qrow_off[k] * D)[col]);
+                const float2 f = __bfloat1622float2(
+                    *reinterpret_cast<const __nv_bfloat162*>(&qw[k][j]));
                 __half2 hv = __floats2half2_rn(f.x * up[k], f.y * up[k]);
                 v[2 * i + k] = *reinterpret_cast<uint32_t*>(&hv);
               }
@@ -789,18 +794,24 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
     while (ok && iter.next(s)) {
       for (int it = s.i0; it < s.i1; ++it, ++g) {
         const int r = g % kRing, st = g % kStages, vst = g % kVStages;
-        ok = sync.wait(smem_u32(&sh->ring_full[r]), (g / kRing) & 1);
-        if (!ok) break;
+        const uint32_t ph = (g / kRing) & 1;
         const uint8_t* stage = ring + r * C::kRingStage;
-        ok = sync.wait(smem_u32(&sh->k_free[st]), ((g / kStages) & 1) ^ 1);
+        // K codes -> fp16 K tile; the QK of the tile may start at once
+        ok = sync.wait(smem_u32(&sh->ring_full[0][r]), ph) &&
+             sync.wait(smem_u32(&sh->k_free[st]), ((g / kStages) & 1) ^ 1);
         if (!ok) break;
         convert_codes<D>(stage, kbuf + st * C::kTileBytes, lt);
-        ok = sync.wait(smem_u32(&sh->v_free[vst]), ((g / kVStages) & 1) ^ 1);
+        mbar_arrive(smem_u32(&sh->ring_empty[0][r]));
+        fence_async_smem();
+        mbar_arrive(smem_u32(&sh->k_full[st]));
+        // V codes -> fp16 V tile
+        ok = sync.wait(smem_u32(&sh->ring_full[1][r]), ph) &&
+             sync.wait(smem_u32(&sh->v_free[vst]), ((g / kVStages) & 1) ^ 1);
         if (!ok) break;
         convert_codes<D>(stage + C::kRingCodes, vbuf + vst * C::kTileBytes, lt);
-        mbar_arrive(smem_u32(&sh->ring_empty[r]));
+        mbar_arrive(smem_u32(&sh->ring_empty[1][r]));
         fence_async_smem();
-        mbar_arrive(smem_u32(&sh->kv_full[st]));
+        mbar_arrive(smem_u32(&sh->v_full[vst]));
       }
     }
   } else if (warp >= kProducerWarp) {
@@ -812,16 +823,24 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
     while (ok && iter.next(s)) {
       for (int it = s.i0; it < s.i1; ++it, ++g) {
         const int r = g % kRing, vst = g % kVStages;
-        if (lane == 0) {
-          // ring stage free (converted), scale stage free (read by the softmax
-          // of the tile three back)
-          ok = sync.wait(smem_u32(&sh->ring_empty[r]), ((g / kRing) & 1) ^ 1) &&
-               sync.wait(smem_u32(&sh->sc_free[vst]), ((g / kVStages) & 1) ^ 1);
-        }
+        const uint32_t ph = ((g / kRing) & 1) ^ 1;
+        uint8_t* stage = ring + r * C::kRingStage;
+        // K codes once the converters are done with the K codes of tile g - 2
+        if (lane == 0) ok = sync.wait(smem_u32(&sh->ring_empty[0][r]), ph);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
-        stage_tile<D>(p, s, it, ring + r * C::kRingStage, scales + vst * 2 * kTileKeys,
-                      smem_u32(&sh->ring_full[r]), smem_u32(&sh->sc_full[vst]), lane, win);
+        const int page = stage_codes<D>(p, s, it, p.k_pages, stage, smem_u32(&sh->ring_full[0][r]),
+                                        lane, win);
+        // V codes and the scales once the converters are done with the V codes
+        // of tile g - 2 and the softmax with the scales of tile g - 3
+        if (lane == 0)
+          ok = sync.wait(smem_u32(&sh->ring_empty[1][r]), ph) &&
+               sync.wait(smem_u32(&sh->sc_free[vst]), ((g / kVStages) & 1) ^ 1);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        stage_codes<D>(p, s, it, p.v_pages, stage + C::kRingCodes, smem_u32(&sh->ring_full[1][r]),
+                       lane, win);
+        stage_scales(p, s, page, scales + vst * 2 * kTileKeys, smem_u32(&sh->sc_full[vst]), lane);
       }
     }
   } else {
@@ -855,7 +874,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
           if (is_qk) {
             if (st != qk_par) continue;
             ok = sync.wait(smem_u32(&sh->p_free[st]), ((g / kStages) & 1) ^ 1) &&
-                 sync.wait(smem_u32(&sh->kv_full[st]), (g / kStages) & 1);
+                 sync.wait(smem_u32(&sh->k_full[st]), (g / kStages) & 1);
             if (!ok) break;
             fence_after();
 #pragma unroll
@@ -867,7 +886,8 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
             mma_commit(smem_u32(&sh->s_full[st]));
             mma_commit(smem_u32(&sh->k_free[st]));
           } else {
-            ok = sync.wait(smem_u32(&sh->p_full[st]), (g / kStages) & 1);
+            ok = sync.wait(smem_u32(&sh->p_full[st]), (g / kStages) & 1) &&
+                 sync.wait(smem_u32(&sh->v_full[vst]), (g / kVStages) & 1);
             if (!ok) break;
             fence_after();
 #pragma unroll
