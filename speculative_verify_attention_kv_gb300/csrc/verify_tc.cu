@@ -236,7 +236,7 @@ __device__ __forceinline__ void tmem_st16x256_x8(uint32_t taddr, const uint32_t 
       ::"r"(taddr), SPLASH_W8(0), SPLASH_W8(8), SPLASH_W8(16), SPLASH_W8(24)
       : "memory");
 }
-// 16 lanes x 32 columns (16x128b, 16 repetitions): repetition i holds column
+// 16 lanes x 64 columns (16x128b, 16 repetitions): repetition i holds column
 // 4i + t%4 of lane base + t/4 (v[2i]) and of lane base + 8 + t/4 (v[2i+1])
 __device__ __forceinline__ void tmem_st16x128_x16(uint32_t taddr, const uint32_t (&v)[32]) {
   asm volatile(
@@ -244,6 +244,14 @@ __device__ __forceinline__ void tmem_st16x128_x16(uint32_t taddr, const uint32_t
       "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
       "%28, %29, %30, %31, %32};"
       ::"r"(taddr), SPLASH_W8(0), SPLASH_W8(8), SPLASH_W8(16), SPLASH_W8(24)
+      : "memory");
+}
+// 16 lanes x 32 columns (16x128b, 8 repetitions), same layout as above
+__device__ __forceinline__ void tmem_st16x128_x8(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.16x128b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16};"
+      ::"r"(taddr), SPLASH_W8(0), SPLASH_W8(8)
       : "memory");
 }
 __device__ __forceinline__ void tmem_wait_ld() {
@@ -578,25 +586,23 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
           up[k] = __uint_as_float((uint32_t)(e + 127) << 23);
           rowfac[k] = p.sm_scale_log2 / up[k];
         }
+        static_assert((D / 2) % 64 == 0, "Q' stores of 64 packed columns");
 #pragma unroll
-        for (int c0 = 0; c0 < D / 2; c0 += 64) {          // 64 packed columns per pass
+        for (int c0 = 0; c0 < D / 2; c0 += 64) {          // 64 packed columns per store
+          uint32_t v[32];
 #pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            uint32_t v[32];
+          for (int i = 0; i < 16; ++i) {
+            // packed column c0 + 4i + quad holds d pair 8j + 2*quad, j = c0/4 + i
+            const int j = c0 / 4 + i;
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              // packed column c0 + 32*half + 4i + quad holds d pair 8j + 2*quad
-              const int j = (c0 + 32 * half) / 4 + i;
-#pragma unroll
-              for (int k = 0; k < 2; ++k) {
-                const float2 f = __bfloat1622float2(
-                    *reinterpret_cast<const __nv_bfloat162*>(&qw[k][j]));
-                __half2 hv = __floats2half2_rn(f.x * up[k], f.y * up[k]);
-                v[2 * i + k] = *reinterpret_cast<uint32_t*>(&hv);
-              }
+            for (int k = 0; k < 2; ++k) {
+              const float2 f =
+                  __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&qw[k][j]));
+              __half2 hv = __floats2half2_rn(f.x * up[k], f.y * up[k]);
+              v[2 * i + k] = *reinterpret_cast<uint32_t*>(&hv);
             }
-            tmem_st16x128_x16(tmem + lane_base + C::kQCol + c0 + 32 * half, v);
           }
+          tmem_st16x128_x16(tmem + lane_base + C::kQCol + c0, v);
         }
         tmem_wait_st();
       }
@@ -610,7 +616,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
              sync.wait(smem_u32(&sh->s_full[st]), (g / kStages) & 1);
         if (!ok) break;
         fence_after();
-        uint32_t pw[32];
+        uint32_t pw[16];                                   // P: 32 packed columns
         float alpha[2] = {1.f, 1.f};
         if (warp_live) {
           const int k0 = it * kTileKeys;
@@ -728,7 +734,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
         }
         mbar_arrive(smem_u32(&sh->sc_free[vst]));          // scales of this tile are read
         if (warp_live) {
-          tmem_st16x128_x16(tmem + lane_base + C::kSCol + st * kTileKeys, pw);
+          tmem_st16x128_x8(tmem + lane_base + C::kSCol + st * kTileKeys, pw);
           tmem_wait_st();
         }
         fence_before();
