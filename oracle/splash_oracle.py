@@ -37,6 +37,10 @@ here (the same ones the CUDA path implements):
   log of sum(exp(scores)), sm_scale included.
 * attention_partial / lse_combine: the split-KV form of the same quantity,
   partial (o_i, lse_i) over a key range, merged by log-sum-exp weights.
+* sliding window (the draft's windowed attention, section "옵션이 아니라 기본
+  경로인 DFlash 2 추측 디코딩"): with window W > 0, verify token t sees only the W
+  most recent keys up to its own position, ctx + t - W < j <= ctx + t;
+  W = 0 means no lower bound.
 * accept_commit: each request advances by the tokens it accepted (same
   section of the discuss.pytorch.kr article). Reading: block x_0..x_{T-1}
   (x_0 = the target's previous output, x_1.. = drafts), target choices
@@ -136,9 +140,13 @@ def gather_keys(pool: PagedPool, page_table_row: np.ndarray, h: int, n: int):
 # ---------------------------------------------------------------------------
 # attention
 # ---------------------------------------------------------------------------
-def _visible(j: np.ndarray, ctx: int, t: int) -> np.ndarray:
-    """Key j is visible to verify token t iff j <= ctx + t."""
-    return j <= ctx + t
+def _visible(j: np.ndarray, ctx: int, t: int, window: int = 0) -> np.ndarray:
+    """Key j is visible to verify token t iff j <= ctx + t (and, with a
+    window W > 0, j > ctx + t - W)."""
+    vis = j <= ctx + t
+    if window > 0:
+        vis = vis & (j > ctx + t - window)
+    return vis
 
 
 def _softmax_rows(scores: np.ndarray, visible: np.ndarray):
@@ -150,7 +158,8 @@ def _softmax_rows(scores: np.ndarray, visible: np.ndarray):
     return e / z, (m + np.log(z))[..., 0]
 
 
-def attention_seq_head(q: np.ndarray, k: np.ndarray, v: np.ndarray, ctx: int, sm_scale: float):
+def attention_seq_head(q: np.ndarray, k: np.ndarray, v: np.ndarray, ctx: int, sm_scale: float,
+                       window: int = 0):
     """Verify attention of one sequence and one KV head.
 
     q: fp64 [T, G, D] (bf16 values); k, v: fp64 [ctx + T, D] (dequantised).
@@ -160,13 +169,14 @@ def attention_seq_head(q: np.ndarray, k: np.ndarray, v: np.ndarray, ctx: int, sm
     n = k.shape[0]
     scores = float(np.float32(sm_scale)) * (q.reshape(T * G, D) @ k.T)   # [T*G, n]
     j = np.arange(n)
-    vis = np.stack([_visible(j, ctx, t) for t in range(T) for _ in range(G)])
+    vis = np.stack([_visible(j, ctx, t, window) for t in range(T) for _ in range(G)])
     p, lse = _softmax_rows(scores, vis)
     return (p @ v).reshape(T, G, D), lse.reshape(T, G)
 
 
 def attention(q: np.ndarray, pool: PagedPool, page_table: np.ndarray, context_lens: np.ndarray,
-              block_lens: np.ndarray, num_kv_heads: int, sm_scale: float, seqs=None):
+              block_lens: np.ndarray, num_kv_heads: int, sm_scale: float, seqs=None,
+              window: int = 0):
     """Verify attention for every (sequence, KV head) (or the listed sequences).
 
     q: float [sum(block_lens), Hq, D] holding bf16 values. Returns O fp64
@@ -186,14 +196,14 @@ def attention(q: np.ndarray, pool: PagedPool, page_table: np.ndarray, context_le
         for h in range(num_kv_heads):
             k, v = gather_keys(pool, page_table[b], h, ctx + T)
             qs = q[r0:r0 + T, h * G:(h + 1) * G, :]
-            o, l = attention_seq_head(qs, k, v, ctx, sm_scale)
+            o, l = attention_seq_head(qs, k, v, ctx, sm_scale, window)
             out[r0:r0 + T, h * G:(h + 1) * G, :] = o
             lse[r0:r0 + T, h * G:(h + 1) * G] = l
     return out, lse
 
 
 def attention_partial(q: np.ndarray, k: np.ndarray, v: np.ndarray, ctx: int, sm_scale: float,
-                      k0: int, k1: int):
+                      k0: int, k1: int, window: int = 0):
     """Split-KV partial over keys [k0, k1) of one sequence and KV head.
 
     Returns o_i fp64 [T, G, D] (normalised by its own sum) and lse_i [T, G]
@@ -202,7 +212,7 @@ def attention_partial(q: np.ndarray, k: np.ndarray, v: np.ndarray, ctx: int, sm_
     T, G, D = q.shape
     scores = float(np.float32(sm_scale)) * (q.reshape(T * G, D) @ k[k0:k1].T)
     j = np.arange(k0, k1)
-    vis = np.stack([_visible(j, ctx, t) for t in range(T) for _ in range(G)])
+    vis = np.stack([_visible(j, ctx, t, window) for t in range(T) for _ in range(G)])
     o = np.zeros((T * G, D))
     lse = np.full(T * G, -np.inf)
     any_vis = vis.any(axis=1)

@@ -140,6 +140,67 @@ def test_attention_matches_sdpa_on_truncated_keys(ctx, T, hq, hkv, D):
     assert np.max(np.abs(lse - rl)) < 1e-12
 
 
+def _sdpa_window(W, pool, q, window):
+    """Row (t, hq) = unmasked attention over keys max(0, ctx+t-W+1) .. ctx+t."""
+    s = W.spec
+    G = s.group
+    o = np.zeros(q.shape)
+    lse = np.zeros(q.shape[:2])
+    sm = float(W.sm_scale)
+    for b in range(W.num_seqs):
+        ctx, T = int(W.context_lens[b]), int(W.block_lens[b])
+        for h in range(s.num_kv_heads):
+            K, V = _dense_kv(pool, W.page_table[b], h, ctx + T)
+            for t in range(T):
+                row = int(W.q_offsets[b]) + t
+                qq = torch.tensor(q[row, h * G:(h + 1) * G], dtype=torch.float64)
+                hi = ctx + t + 1
+                lo = max(0, hi - window)
+                out = torch.nn.functional.scaled_dot_product_attention(
+                    qq[None], K[None, lo:hi], V[None, lo:hi], scale=sm)[0]
+                o[row, h * G:(h + 1) * G] = out.numpy()
+                lse[row, h * G:(h + 1) * G] = torch.logsumexp(sm * qq @ K[lo:hi].T, dim=-1).numpy()
+    return o, lse
+
+
+@pytest.mark.parametrize("window", [1, 2, 5, 17, 40, 1000])
+def test_window_matches_sdpa_on_window_keys(window):
+    W = wl.custom(8, 2, 16, [37, 0, 20], [4, 3, 16], seed=5)
+    pool = oracle_pool(W)
+    q = q_values(W)
+    o, lse = O.attention(q, pool, W.page_table, W.context_lens, W.block_lens,
+                         W.spec.num_kv_heads, float(W.sm_scale), window=window)
+    ro, rl = _sdpa_window(W, pool, q, window)
+    assert np.max(np.abs(o - ro)) < 1e-12 and np.max(np.abs(lse - rl)) < 1e-12
+
+
+def test_window_one_is_the_diagonal_key():
+    W = wl.custom(4, 2, 16, [9], [3], seed=6)
+    pool = oracle_pool(W)
+    q = q_values(W)
+    o, lse = O.attention(q, pool, W.page_table, W.context_lens, W.block_lens, 2,
+                         float(W.sm_scale), window=1)
+    for t in range(3):
+        j = 9 + t
+        p, sl = int(W.page_table[0, j // 16]), j % 16
+        for hq in range(4):
+            h = hq // 2
+            k = pool.k_codes[p, h, sl].astype(np.float64) * float(pool.k_scales[p, h, sl])
+            v = pool.v_codes[p, h, sl].astype(np.float64) * float(pool.v_scales[p, h, sl])
+            assert np.max(np.abs(o[t, hq] - v)) < 1e-15
+            assert abs(lse[t, hq] - float(W.sm_scale) * (q[t, hq] @ k)) < 1e-12
+
+
+def test_window_covering_everything_is_full_attention():
+    W = wl.custom(8, 2, 16, [37, 5], [4, 3], seed=7)
+    pool = oracle_pool(W)
+    q = q_values(W)
+    full = O.attention(q, pool, W.page_table, W.context_lens, W.block_lens, 2, float(W.sm_scale))
+    win = O.attention(q, pool, W.page_table, W.context_lens, W.block_lens, 2, float(W.sm_scale),
+                      window=41)
+    assert np.array_equal(full[0], win[0]) and np.array_equal(full[1], win[1])
+
+
 def test_tiny_workload_matches_sdpa():
     W = wl.make("tiny")
     pool = oracle_pool(W)
@@ -345,13 +406,20 @@ def test_planted_multiply_form_is_caught(monkeypatch):
 
 
 def test_planted_mask_off_by_one_is_caught(monkeypatch):
-    monkeypatch.setattr(O, "_visible", lambda j, ctx, t: j < ctx + t)
+    monkeypatch.setattr(O, "_visible", lambda j, ctx, t, window=0: j < ctx + t)
     assert _pins_fail(lambda: test_attention_matches_sdpa_on_truncated_keys([37], [4], 8, 2, 32))
 
 
 def test_planted_mask_too_wide_is_caught(monkeypatch):
-    monkeypatch.setattr(O, "_visible", lambda j, ctx, t: j <= ctx + t + 1)
+    monkeypatch.setattr(O, "_visible", lambda j, ctx, t, window=0: j <= ctx + t + 1)
     assert _pins_fail(test_future_keys_do_not_matter_and_the_diagonal_does)
+
+
+def test_planted_window_off_by_one_is_caught(monkeypatch):
+    # a window of W keys that starts one key early (W + 1 keys)
+    monkeypatch.setattr(O, "_visible",
+                        lambda j, ctx, t, window=0: (j <= ctx + t) & ((window <= 0) | (j >= ctx + t - window)))
+    assert _pins_fail(lambda: test_window_matches_sdpa_on_window_keys(5))
 
 
 def test_planted_dequant_mistake_is_caught(monkeypatch):
@@ -362,8 +430,8 @@ def test_planted_dequant_mistake_is_caught(monkeypatch):
 def test_planted_gqa_mistake_is_caught(monkeypatch):
     orig = O.attention_seq_head
 
-    def swapped(q, k, v, ctx, sm):      # query heads of a group paired with the wrong rows
-        return orig(q[:, ::-1], k, v, ctx, sm)
+    def swapped(q, k, v, ctx, sm, window=0):      # query heads paired with the wrong rows
+        return orig(q[:, ::-1], k, v, ctx, sm, window)
     monkeypatch.setattr(O, "attention_seq_head", swapped)
     assert _pins_fail(lambda: test_attention_matches_sdpa_on_truncated_keys([37], [4], 8, 2, 32))
 
