@@ -199,6 +199,28 @@ int splash_verify_attention_tuned(const uint16_t* q, int num_q_tokens,
                                   struct CUstream_st* stream, int path, int ctas_per_class);
 
 /*
+ * splash_verify_attention_swa — splash_verify_attention_tuned with a sliding
+ * window: verify token t of sequence b sees only the `window` most recent keys
+ * up to its own position, context_lens[b] + t - window < j <= context_lens[b]
+ * + t (the draft model's windowed attention, "옵션이 아니라 기본 경로인 DFlash 2
+ * 추측 디코딩" section of the Splash article on discuss.pytorch.kr). window = 0
+ * is the full mask of splash_verify_attention; window < 0 is an argument error.
+ * Page-table entries of pages that lie wholly below key
+ * context_lens[b] - window + 1 are never read (they may be -1). Same output,
+ * workspace, determinism and error contract as splash_verify_attention.
+ */
+int splash_verify_attention_swa(const uint16_t* q, int num_q_tokens,
+                                const int8_t* k_pages, const int8_t* v_pages,
+                                const float* k_scales, const float* v_scales,
+                                const int32_t* page_table, int max_pages_per_seq,
+                                const int32_t* context_lens, const int32_t* block_lens,
+                                int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                int page_size, int num_pages, int max_block_len, float sm_scale,
+                                int window, uint16_t* out, float* lse, void* workspace,
+                                size_t workspace_bytes, int* device_status,
+                                struct CUstream_st* stream, int path, int ctas_per_class);
+
+/*
  * splash_verify_attention_profiled — splash_verify_attention_tuned that also
  * records two caller-created CUDA events on `stream`: `attn_begin` just before
  * the attention kernel launch(es) and `attn_end` just after, so that the

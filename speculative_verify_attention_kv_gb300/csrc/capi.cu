@@ -14,7 +14,7 @@ cudaError_t launch_kv_append_bf16(const __nv_bfloat16*, const __nv_bfloat16*, in
 cudaError_t launch_accept_commit(const int32_t*, const int32_t*, int, const int32_t*, int32_t*,
                                  int32_t*, int32_t*, int, int*, cudaStream_t);
 cudaError_t launch_plan(const int32_t*, const int32_t*, int, int, int, int, int, int, int, int,
-                        int, int, int, int, unsigned char*, int*, cudaStream_t);
+                        int, int, int, int, int, unsigned char*, int*, cudaStream_t);
 cudaError_t launch_combine(int, int, int, int, int, int, int, const unsigned char*,
                            __nv_bfloat16*, float*, cudaStream_t);
 cudaError_t launch_verify_simt(const AttnParams&, int, int, cudaStream_t);
@@ -172,18 +172,21 @@ size_t splash_verify_attention_workspace_size(int num_seqs, int num_q_tokens, in
                              max_block_len, sms, 4 * sms);
 }
 
-int splash_verify_attention_profiled(
+}  // extern "C"
+
+// All attention entry points: window 0 is the full block-causal mask.
+static int verify_impl(
     const uint16_t* q, int num_q_tokens, const int8_t* k_pages, const int8_t* v_pages,
     const float* k_scales, const float* v_scales, const int32_t* page_table,
     int max_pages_per_seq, const int32_t* context_lens, const int32_t* block_lens, int num_seqs,
     int num_q_heads, int num_kv_heads, int head_dim, int page_size, int num_pages,
-    int max_block_len, float sm_scale, uint16_t* out, float* lse, void* workspace,
+    int max_block_len, float sm_scale, int window, uint16_t* out, float* lse, void* workspace,
     size_t workspace_bytes, int* device_status, struct CUstream_st* stream, int path,
     int ctas_per_class, struct CUevent_st* attn_begin, struct CUevent_st* attn_end) {
   int st = check_attn_shape(num_q_tokens, num_seqs, num_q_heads, num_kv_heads, head_dim,
                             page_size, max_block_len, max_pages_per_seq);
   if (st != SPLASH_OK) return st;
-  if (path < 0 || path > 2 || ctas_per_class < 0 || num_pages < 0)
+  if (path < 0 || path > 2 || ctas_per_class < 0 || num_pages < 0 || window < 0)
     return SPLASH_ERR_INVALID_ARGUMENT;
   if (num_q_tokens == 0 || num_seqs == 0) return SPLASH_OK;
   if (!q || !k_pages || !v_pages || !k_scales || !v_scales || !page_table || !context_lens ||
@@ -221,7 +224,7 @@ int splash_verify_attention_profiled(
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = launch_plan(context_lens, block_lens, num_seqs, num_kv_heads, G,
                               max_pages_per_seq, max_block_len, kTcTile, kSimtTile, nt, ns, path,
-                              (int)rb, num_q_tokens, ws, device_status, s);
+                              (int)rb, num_q_tokens, window, ws, device_status, s);
   if (e != cudaSuccess) return SPLASH_ERR_CUDA;
 
   AttnParams p;
@@ -239,6 +242,7 @@ int splash_verify_attention_profiled(
   p.head_dim = head_dim;
   p.num_pages = num_pages;
   p.sm_scale_log2 = sm_scale * 1.4426950408889634f;
+  p.window = window;
   p.out = reinterpret_cast<__nv_bfloat16*>(out);
   p.lse = lse;
   p.ws = ws;
@@ -258,6 +262,40 @@ int splash_verify_attention_profiled(
   e = launch_combine(num_q_tokens, num_q_heads, num_seqs, num_kv_heads, G, head_dim, (int)rb, ws,
                      p.out, lse, s);
   return e == cudaSuccess ? SPLASH_OK : SPLASH_ERR_CUDA;
+}
+
+extern "C" {
+
+int splash_verify_attention_profiled(
+    const uint16_t* q, int num_q_tokens, const int8_t* k_pages, const int8_t* v_pages,
+    const float* k_scales, const float* v_scales, const int32_t* page_table,
+    int max_pages_per_seq, const int32_t* context_lens, const int32_t* block_lens, int num_seqs,
+    int num_q_heads, int num_kv_heads, int head_dim, int page_size, int num_pages,
+    int max_block_len, float sm_scale, uint16_t* out, float* lse, void* workspace,
+    size_t workspace_bytes, int* device_status, struct CUstream_st* stream, int path,
+    int ctas_per_class, struct CUevent_st* attn_begin, struct CUevent_st* attn_end) {
+  return verify_impl(q, num_q_tokens, k_pages, v_pages, k_scales, v_scales, page_table,
+                     max_pages_per_seq, context_lens, block_lens, num_seqs, num_q_heads,
+                     num_kv_heads, head_dim, page_size, num_pages, max_block_len, sm_scale, 0, out,
+                     lse, workspace, workspace_bytes, device_status, stream, path, ctas_per_class,
+                     attn_begin, attn_end);
+}
+
+int splash_verify_attention_swa(const uint16_t* q, int num_q_tokens, const int8_t* k_pages,
+                                const int8_t* v_pages, const float* k_scales,
+                                const float* v_scales, const int32_t* page_table,
+                                int max_pages_per_seq, const int32_t* context_lens,
+                                const int32_t* block_lens, int num_seqs, int num_q_heads,
+                                int num_kv_heads, int head_dim, int page_size, int num_pages,
+                                int max_block_len, float sm_scale, int window, uint16_t* out,
+                                float* lse, void* workspace, size_t workspace_bytes,
+                                int* device_status, struct CUstream_st* stream, int path,
+                                int ctas_per_class) {
+  return verify_impl(q, num_q_tokens, k_pages, v_pages, k_scales, v_scales, page_table,
+                     max_pages_per_seq, context_lens, block_lens, num_seqs, num_q_heads,
+                     num_kv_heads, head_dim, page_size, num_pages, max_block_len, sm_scale, window,
+                     out, lse, workspace, workspace_bytes, device_status, stream, path,
+                     ctas_per_class, nullptr, nullptr);
 }
 
 int splash_verify_attention_tuned(const uint16_t* q, int num_q_tokens, const int8_t* k_pages,

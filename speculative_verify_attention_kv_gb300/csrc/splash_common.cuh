@@ -33,9 +33,24 @@ struct PlanHeader {
   int group;                      // G = Hq / Hkv
   int total_part_rows;            // partial rows the split units use
   int rows_bound;                 // capacity of the partial buffers (rows)
-  int pad_[5];
+  int window;                     // sliding window W (0: none)
+  int pad_[4];
 };
 static_assert(sizeof(PlanHeader) == 64, "header size");
+
+// First key a unit (context ctx) needs: with a sliding window W > 0, verify
+// token t sees keys ctx + t - W < j <= ctx + t, so no row sees a key below
+// ctx - W + 1; tiles wholly below it are skipped and their pages never read.
+__host__ __device__ inline int unit_first_key(int ctx, int window) {
+  return window > 0 ? (ctx - window + 1 > 0 ? ctx - window + 1 : 0) : 0;
+}
+// Key tiles of a unit: [first, first + count) of tile_keys keys each.
+__host__ __device__ inline int unit_first_tile(int ctx, int window, int tile_keys) {
+  return unit_first_key(ctx, window) / tile_keys;
+}
+__host__ __device__ inline int unit_tiles(int ctx, int T, int window, int tile_keys) {
+  return (ctx + T + tile_keys - 1) / tile_keys - unit_first_tile(ctx, window, tile_keys);
+}
 
 // Byte offsets of the workspace regions (all 256-aligned).
 struct WorkspaceLayout {
@@ -96,6 +111,7 @@ struct AttnParams {
   int head_dim;
   int num_pages;
   float sm_scale_log2;            // sm_scale * log2(e)
+  int window;                     // sliding window W (0: none); the planner has the same value
   __nv_bfloat16* out;
   float* lse;
   unsigned char* ws;

@@ -1,7 +1,8 @@
 // Split plan and log-sum-exp combine of split-KV verify attention.
 //
 // Work unit = (sequence b, KV head h): its T_b*G query rows against keys
-// 0 .. ctx_b + T_b - 1. Each unit is cut into key tiles; the tiles of all units
+// 0 .. ctx_b + T_b - 1 (with a sliding window W, from the tile holding key
+// ctx_b - W + 1 on). Each unit is cut into key tiles; the tiles of all units
 // of one class (tensor-core or CUDA-core kernel) form one stream that is split
 // evenly over that kernel's persistent CTAs. A unit touched by one CTA is
 // finished by it; a unit touched by n > 1 CTAs leaves n partials (o_i
@@ -45,7 +46,7 @@ __global__ void __launch_bounds__(kPlanThreads)
 plan_kernel(const int32_t* __restrict__ context_lens, const int32_t* __restrict__ block_lens,
             int num_seqs, int num_kv_heads, int group, int max_pages, int max_block_len,
             int tile_tc, int tile_simt, int ncta_tc, int ncta_simt, int path, int rows_bound,
-            int num_q_tokens, unsigned char* ws, int* device_status) {
+            int num_q_tokens, int window, unsigned char* ws, int* device_status) {
   __shared__ int s_warp[32];
   const WorkspaceLayout L = make_layout(num_seqs, num_kv_heads, 0, rows_bound);
   int* q_off = reinterpret_cast<int*>(ws + L.q_off);
@@ -78,7 +79,7 @@ plan_kernel(const int32_t* __restrict__ context_lens, const int32_t* __restrict_
         const int rows = T * group;
         cls = path == 1 ? kClassSimt : path == 2 ? kClassTensor
                         : (rows >= kTensorMinRows ? kClassTensor : kClassSimt);
-        tiles = (ctx + T + tile[cls] - 1) / tile[cls];
+        tiles = unit_tiles(ctx, T, window, tile[cls]);
       }
       seq_T[b] = T;
       seq_ctx[b] = ctx;
@@ -127,7 +128,7 @@ plan_kernel(const int32_t* __restrict__ context_lens, const int32_t* __restrict_
       int ns = 0, cf = 0;
       if (cls >= 0) {
         const int T = seq_T[b], ctx = seq_ctx[b];
-        const int tiles = (ctx + T + tile[cls] - 1) / tile[cls];
+        const int tiles = unit_tiles(ctx, T, window, tile[cls]);
         const int tp = stp[cls * (num_seqs + 1) + b] + h * tiles;
         cf = cta_of_tile(tp, total[cls], ncta_eff[cls]);
         const int cl = cta_of_tile(tp + tiles - 1, total[cls], ncta_eff[cls]);
@@ -155,6 +156,7 @@ plan_kernel(const int32_t* __restrict__ context_lens, const int32_t* __restrict_
     hd->group = group;
     hd->total_part_rows = run_rows;
     hd->rows_bound = rows_bound;
+    hd->window = window;
   }
 }
 
@@ -218,12 +220,12 @@ lse_combine_kernel(int num_q_tokens, int num_q_heads, int num_seqs, int num_kv_h
 cudaError_t launch_plan(const int32_t* context_lens, const int32_t* block_lens, int num_seqs,
                         int num_kv_heads, int group, int max_pages, int max_block_len, int tile_tc,
                         int tile_simt, int ncta_tc, int ncta_simt, int path, int rows_bound,
-                        int num_q_tokens, unsigned char* ws, int* device_status,
+                        int num_q_tokens, int window, unsigned char* ws, int* device_status,
                         cudaStream_t stream) {
   plan_kernel<<<1, kPlanThreads, 0, stream>>>(context_lens, block_lens, num_seqs, num_kv_heads,
                                               group, max_pages, max_block_len, tile_tc, tile_simt,
                                               ncta_tc, ncta_simt, path, rows_bound, num_q_tokens,
-                                              ws, device_status);
+                                              window, ws, device_status);
   return cudaGetLastError();
 }
 

@@ -60,6 +60,7 @@ verify_simt_kernel(AttnParams p, int rows_cap) {
 
   const int total = hd->total_tiles[kClassSimt];
   const int ncta = hd->ncta[kClassSimt];
+  const int window = hd->window;
   if ((int)blockIdx.x >= ncta) return;
   int t = tile_begin(blockIdx.x, total, ncta);
   const int t_end = tile_begin(blockIdx.x + 1, total, ncta);
@@ -68,11 +69,13 @@ verify_simt_kernel(AttnParams p, int rows_cap) {
     const int b = upper_index(stp, B - 1, t);
     const int T = seq_T[b], ctx = seq_ctx[b];
     const int Lk = ctx + T;
-    const int tiles = (Lk + TK - 1) / TK;
+    const int klo = unit_first_key(ctx, window);           // keys below are never visible
+    const int first = unit_first_tile(ctx, window, TK);
+    const int tiles = unit_tiles(ctx, T, window, TK);
     const int local = t - stp[b];
     const int h = local / tiles;
-    const int i0 = local % tiles;
-    const int i1 = min(tiles, i0 + (t_end - t));
+    const int i0 = first + local % tiles;
+    const int i1 = min(first + tiles, i0 + (t_end - t));
     const int R = T * G;
     const int u = b * Hkv + h;
     const int32_t* ptab = p.page_table + (size_t)b * p.max_pages_per_seq;
@@ -102,7 +105,7 @@ verify_simt_kernel(AttnParams p, int rows_cap) {
         const int jj = rem / (D / 16), c = rem % (D / 16);
         const int j = k0 + jj;
         uint4 val = make_uint4(0, 0, 0, 0);
-        if (j < Lk) {
+        if (j < Lk && j >= klo) {
           const int page = ptab[j / kPageSize];
           if (page >= 0 && page < p.num_pages) {
             const int8_t* base = (which ? p.v_pages : p.k_pages) +
@@ -115,7 +118,7 @@ verify_simt_kernel(AttnParams p, int rows_cap) {
       for (int jj = tid; jj < 2 * TK; jj += kSimtThreads) {
         const int which = jj / TK, j = k0 + jj % TK;
         float sc = 0.f;
-        if (j < Lk) {
+        if (j < Lk && j >= klo) {
           const int page = ptab[j / kPageSize];
           if (page >= 0 && page < p.num_pages) {
             const float* sp = which ? p.v_scales : p.k_scales;
@@ -132,7 +135,7 @@ verify_simt_kernel(AttnParams p, int rows_cap) {
       for (int idx = tid; idx < R * TK; idx += kSimtThreads) {
         const int jj = idx / R, r = idx % R;
         const int j = k0 + jj;
-        const bool vis = (j < Lk) && (j <= ctx + r / G);
+        const bool vis = (j < Lk) && (j <= ctx + r / G) && (window <= 0 || j > ctx + r / G - window);
         float dot = 0.f;
         const __nv_bfloat16* qr = q_s + (size_t)r * SM::kQStride;
         const int8_t* kr = k_s + jj * SM::kKStride;

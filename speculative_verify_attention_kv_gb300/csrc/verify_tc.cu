@@ -277,13 +277,14 @@ __device__ __forceinline__ void i8x4_to_h2x2(uint32_t w, uint32_t& lo, uint32_t&
 // ------------------------------------------------------------- work iteration
 struct Seg {
   int b, h, i0, i1, T, ctx, Lk, R, u;
+  int klo;                        // first key any row of the unit sees
 };
 
 struct SegIter {
   const int* stp;
   const int* seq_T;
   const int* seq_ctx;
-  int B, G, Hkv;
+  int B, G, Hkv, window;
   int t, t_end;
   __device__ bool next(Seg& s) {
     if (t >= t_end) return false;
@@ -291,11 +292,13 @@ struct SegIter {
     s.T = seq_T[s.b];
     s.ctx = seq_ctx[s.b];
     s.Lk = s.ctx + s.T;
-    const int tiles = (s.Lk + kTileKeys - 1) / kTileKeys;
+    s.klo = unit_first_key(s.ctx, window);
+    const int first = unit_first_tile(s.ctx, window, kTileKeys);
+    const int tiles = unit_tiles(s.ctx, s.T, window, kTileKeys);
     const int local = t - stp[s.b];
     s.h = local / tiles;
-    s.i0 = local % tiles;
-    s.i1 = min(tiles, s.i0 + (t_end - t));
+    s.i0 = first + local % tiles;
+    s.i1 = min(first + tiles, s.i0 + (t_end - t));
     s.R = s.T * G;
     s.u = s.b * Hkv + s.h;
     t += s.i1 - s.i0;
@@ -382,7 +385,8 @@ __device__ __forceinline__ int stage_codes(const AttnParams& p, const Seg& s, in
   const int k0 = it * kTileKeys;
   const int npages = (s.Lk + kPageSize - 1) / kPageSize;
   int page = win.get(p, s.b, k0 / kPageSize, npages, lane);
-  const bool needed = k0 + kPageSize * (lane & 3) < s.Lk;
+  const bool needed = k0 + kPageSize * (lane & 3) < s.Lk &&
+                      k0 + kPageSize * ((lane & 3) + 1) > s.klo;
   if (!needed || page >= p.num_pages) page = -1;
   if (needed && page < 0 && lane < kPagesPerTile) report(p.device_status, SPLASH_DEVICE_BAD_PAGE);
   const int mask = (int)(__ballot_sync(0xffffffffu, page >= 0 && lane < kPagesPerTile) &
@@ -451,7 +455,9 @@ __device__ __forceinline__ void convert_codes(const uint8_t* src, uint8_t* dst, 
 }
 
 // ------------------------------------------------------------------- kernel
-template <int D>
+// kSwa: sliding-window instantiation (window read from the parameters); the
+// plain one compiles the window bounds out.
+template <int D, bool kSwa>
 __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
   using C = Cfg<D>;
   static_assert(sizeof(Smem) <= C::kBarBytes, "barrier area");
@@ -522,7 +528,8 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
   const uint32_t tmem = sh->tmem_base;
   const Sync sync{&sh->abort_flag, p.device_status};
 
-  SegIter iter{stp, seq_T, seq_ctx, B, G, Hkv, tile_begin(blockIdx.x, total, ncta),
+  const int window = kSwa ? p.window : 0;
+  SegIter iter{stp, seq_T, seq_ctx, B, G, Hkv, window, tile_begin(blockIdx.x, total, ncta),
                tile_begin(blockIdx.x + 1, total, ncta)};
 
   if (warp < kSoftmaxWarps) {
@@ -544,13 +551,14 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
       ++nsegs;
       const bool warp_live = lb < s.R;
       bool live[2];
-      int lim[2];
+      int lim[2], lo[2];
       size_t qrow_off[2];
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
         live[k] = rr[k] < s.R;
         const int tt = rr[k] / G, gg = rr[k] % G;
         lim[k] = s.ctx + tt;                              // last visible key of the row
+        lo[k] = kSwa ? lim[k] - window + 1 : 0;           // first visible key (with a window)
         qrow_off[k] = (size_t)(q_off[s.b] + tt) * p.num_q_heads + s.h * G + gg;
       }
       float rowfac[2] = {0.f, 0.f};
@@ -642,12 +650,14 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
               x[k][i] = __fmul2_rn(make_float2(__uint_as_float(sv[4 * i + 2 * k]),
                                                __uint_as_float(sv[4 * i + 2 * k + 1])), ks2[i]);
           }
-          int nvis[2];
+          // tile keys jj with nlo <= jj < nvis are visible to the row
+          int nvis[2], nlo[2];
           bool full = true;
 #pragma unroll
           for (int k = 0; k < 2; ++k) {
             nvis[k] = live[k] ? min(kTileKeys, lim[k] - k0 + 1) : 0;
-            full = full && nvis[k] == kTileKeys;
+            nlo[k] = kSwa ? max(lo[k] - k0, -1) : -1;         // compile-time -1 without a window
+            full = full && nvis[k] == kTileKeys && (!kSwa || nlo[k] <= 0);
           }
           if (!full) {
 #pragma unroll
@@ -655,8 +665,8 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
 #pragma unroll
               for (int i = 0; i < 8; ++i) {
                 const int j = 16 * quad + 2 * i;
-                if (j >= nvis[k]) x[k][i].x = -INFINITY;
-                if (j + 1 >= nvis[k]) x[k][i].y = -INFINITY;
+                if (j >= nvis[k] || j < nlo[k]) x[k][i].x = -INFINITY;
+                if (j + 1 >= nvis[k] || j + 1 < nlo[k]) x[k][i].y = -INFINITY;
               }
           }
           float base[2];
@@ -695,8 +705,8 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
               float2 vq = vs2[i];
               if (!full) {      // scales of masked keys are not trusted
                 const int j = 16 * quad + 2 * i;
-                if (j >= nvis[k]) vq.x = 0.f;
-                if (j + 1 >= nvis[k]) vq.y = 0.f;
+                if (j >= nvis[k] || j < nlo[k]) vq.x = 0.f;
+                if (j + 1 >= nvis[k] || j + 1 < nlo[k]) vq.y = 0.f;
               }
               const float2 e0 = __ffma2_rn(x[k][i], rf2, nb2);
               const float2 p0 = make_float2(ex2(e0.x), ex2(e0.y));
@@ -929,17 +939,18 @@ bool tc_supported(int head_dim) { return head_dim == 128 || head_dim == 256; }
 
 cudaError_t launch_verify_tc(const AttnParams& p, int rows_cap, int ncta, cudaStream_t stream) {
   (void)rows_cap;
-#define SPLASH_TC(DD)                                                                          \
+#define SPLASH_TC(DD, SWA)                                                                     \
   do {                                                                                         \
     constexpr int smem = tc::Cfg<DD>::kSmemBytes;                                              \
-    cudaError_t e = cudaFuncSetAttribute(tc::verify_tc_kernel<DD>,                             \
+    cudaError_t e = cudaFuncSetAttribute(tc::verify_tc_kernel<DD, SWA>,                        \
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);   \
     if (e != cudaSuccess) return e;                                                            \
-    tc::verify_tc_kernel<DD><<<ncta, tc::kThreads, smem, stream>>>(p);                        \
+    tc::verify_tc_kernel<DD, SWA><<<ncta, tc::kThreads, smem, stream>>>(p);                   \
   } while (0)
+  const bool swa = p.window > 0;
   switch (p.head_dim) {
-    case 128: SPLASH_TC(128); break;
-    case 256: SPLASH_TC(256); break;
+    case 128: if (swa) SPLASH_TC(128, true); else SPLASH_TC(128, false); break;
+    case 256: if (swa) SPLASH_TC(256, true); else SPLASH_TC(256, false); break;
     default: return cudaErrorNotSupported;
   }
 #undef SPLASH_TC

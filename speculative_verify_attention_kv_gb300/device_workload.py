@@ -85,13 +85,14 @@ class DeviceWorkload:
         sk.splash_kv_append(self.k_new, self.v_new, *self.pool, self.table, self.ctx, self.T,
                             device_status=self.status, stream=stream)
 
-    def attend(self, path=sk.PATH_AUTO, ctas=0, out=None, lse=None, stream=None):
+    def attend(self, path=sk.PATH_AUTO, ctas=0, out=None, lse=None, stream=None, window=0,
+               table=None):
         out = self.out if out is None else out
         lse = self.lse if lse is None else lse
-        sk.splash_verify_attention(self.q, *self.pool, self.table, self.ctx, self.T,
-                                   float(self.W.sm_scale), self.max_T, out, lse, self.ws,
-                                   device_status=self.status, stream=stream, path=path,
-                                   ctas_per_class=ctas)
+        sk.splash_verify_attention(self.q, *self.pool, self.table if table is None else table,
+                                   self.ctx, self.T, float(self.W.sm_scale), self.max_T, out, lse,
+                                   self.ws, device_status=self.status, stream=stream, path=path,
+                                   ctas_per_class=ctas, window=window)
         return out, lse
 
     def step(self, stream=None):

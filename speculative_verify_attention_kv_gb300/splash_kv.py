@@ -52,6 +52,8 @@ def _load() -> ctypes.CDLL:
     lib.splash_verify_attention.argtypes = attn
     lib.splash_verify_attention_tuned.restype = I
     lib.splash_verify_attention_tuned.argtypes = attn + [I, I]
+    lib.splash_verify_attention_swa.restype = I
+    lib.splash_verify_attention_swa.argtypes = attn[:18] + [I] + attn[18:] + [I, I]
     lib.splash_verify_attention_profiled.restype = I
     lib.splash_verify_attention_profiled.argtypes = attn + [I, I, P, P]
     lib.splash_verify_attention_fixed_scratch_bytes.restype = S
@@ -64,6 +66,7 @@ def _load() -> ctypes.CDLL:
 LIB = _load()
 EXPORTED = ("splash_status_string", "splash_abi_version", "splash_tensor_path_supported",
             "splash_kv_append", "splash_kv_append_bf16", "splash_accept_commit",
+            "splash_verify_attention_swa",
             "splash_verify_attention_workspace_size", "splash_verify_attention",
             "splash_verify_attention_tuned", "splash_verify_attention_profiled",
             "splash_verify_attention_fixed_scratch_bytes", "splash_verify_attention_fixed_scratch")
@@ -180,9 +183,10 @@ def alloc_workspace(num_seqs, num_q_tokens, num_q_heads, num_kv_heads, head_dim,
 def splash_verify_attention(q, k_pages, v_pages, k_scales, v_scales, page_table, context_lens,
                             block_lens, sm_scale: float, max_block_len: int, out, lse, workspace,
                             device_status=None, stream=None, path: int = PATH_AUTO,
-                            ctas_per_class: int = 0, events=None) -> None:
+                            ctas_per_class: int = 0, events=None, window: int = 0) -> None:
     """``events``: optional (begin, end) torch.cuda.Event pair recorded around
-    the attention kernels (the profiled entry point)."""
+    the attention kernels (the profiled entry point). ``window`` > 0: sliding
+    window of that many keys (splash_verify_attention_swa)."""
     _check(q, "q", torch.bfloat16, 3)
     _check(out, "out", torch.bfloat16, 3)
     _check(lse, "lse", torch.float32, 2)
@@ -205,7 +209,12 @@ def splash_verify_attention(q, k_pages, v_pages, k_scales, v_scales, page_table,
             context_lens.shape[0], hq, hkv, D, P, num_pages, int(max_block_len), float(sm_scale),
             _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(), _ptr(device_status),
             _stream(stream))
-    if events is not None:
+    if window != 0:
+        if events is not None:
+            raise ValueError("events are recorded only without a window")
+        st = LIB.splash_verify_attention_swa(*args[:18], int(window), *args[18:], int(path),
+                                             int(ctas_per_class))
+    elif events is not None:
         ev = [ctypes.c_void_p(e.cuda_event) if e is not None else None for e in events]
         st = LIB.splash_verify_attention_profiled(*args, int(path), int(ctas_per_class), *ev)
     elif path == PATH_AUTO and ctas_per_class == 0:

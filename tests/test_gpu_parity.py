@@ -28,12 +28,12 @@ from speculative_verify_attention_kv_gb300 import splash_kv as sk  # noqa: E402
 from speculative_verify_attention_kv_gb300 import workloads as wl  # noqa: E402
 
 from common import oracle_pool, q_values  # noqa: E402
-from gpu_common import Run, assert_parity, compare  # noqa: E402
+from gpu_common import Run, assert_parity, assert_parity_scaled, compare  # noqa: E402
 
 
-def oracle_attention(W, pool, seqs=None):
+def oracle_attention(W, pool, seqs=None, window=0):
     return O.attention(q_values(W), pool, W.page_table, W.context_lens, W.block_lens,
-                       W.spec.num_kv_heads, float(W.sm_scale), seqs=seqs)
+                       W.spec.num_kv_heads, float(W.sm_scale), seqs=seqs, window=window)
 
 
 def written_slots(W, seqs):
@@ -365,3 +365,60 @@ def test_empty_batch_is_a_no_op():
     r = Run(W)
     r.attend()
     torch.cuda.synchronize()
+
+
+# ---------------------------------------------------------------------------
+# sliding window
+# ---------------------------------------------------------------------------
+WINDOWS = [1, 7, 64, 65, 200, 1000, 100000]
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("window", WINDOWS)
+def test_sliding_window_matches_oracle(path, window):
+    if not _path_ok(path):
+        pytest.skip("tensor-core kernel not built")
+    W = wl.custom(24, 4, 256, [900, 37, 2100, 0], [16, 1, 8, 5], seed=11)
+    r = Run(W)
+    r.append_block()
+    o_ref, l_ref = oracle_attention(W, oracle_pool(W), window=window)
+    for ctas in (0, 1, 5):
+        o, l = r.attend(path=path, ctas=ctas, window=window)
+        torch.cuda.synchronize()
+        assert_parity_scaled(o, l, o_ref, l_ref, what=f"window {window} path {path} ctas {ctas}")
+    assert int(r.status.item()) == 0
+
+
+def test_sliding_window_never_reads_pages_below_it():
+    # table entries of pages wholly below the window are -1: no error, same result
+    W = wl.custom(24, 4, 256, [1000, 333], [16, 4], seed=12)
+    r = Run(W)
+    r.append_block()
+    window = 100
+    o_ref, l_ref = [t.clone() for t in r.attend(window=window)]
+    table = r.table.clone()
+    for b in range(W.num_seqs):
+        first_key = max(0, int(W.context_lens[b]) - window + 1)
+        table[b, : first_key // 16] = -1
+    torch.cuda.synchronize()
+    o, l = r.attend(window=window, table=table)
+    torch.cuda.synchronize()
+    assert int(r.status.item()) == 0
+    assert torch.equal(o, o_ref) and torch.equal(l, l_ref)
+
+
+def test_window_zero_is_full_attention_bitwise():
+    W, r = _small_run(seed=13)
+    o1, l1 = [t.clone() for t in r.attend()]
+    o2, l2 = [t.clone() for t in r.attend(window=0)]
+    big = int(W.context_lens.max() + W.block_lens.max())
+    o3, l3 = [t.clone() for t in r.attend(window=big)]
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    assert torch.equal(o1, o3) and torch.equal(l1, l3)
+
+
+def test_negative_window_is_an_argument_error():
+    W, r = _small_run(seed=14)
+    with pytest.raises(sk.SplashError) as e:
+        r.attend(window=-1)
+    assert e.value.status == -1
