@@ -32,7 +32,13 @@
  * Shapes and layouts (row-major, innermost last)
  *   Hq = num_q_heads, Hkv = num_kv_heads, G = Hq / Hkv (query head hq uses KV
  *   head hq / G), D = head_dim in {64, 128, 256}, P = page_size = 16.
- *   k_pages, v_pages : int8  [num_pages, Hkv, P, D]   codes
+ *   codes            : int8  one pool [num_pages, Hkv, 2, P, D]; index 0 of the
+ *                      third axis holds K codes, 1 holds V codes, so the K and V
+ *                      codes of a (page, KV head) are one contiguous 2*P*D-byte
+ *                      block. k_pages points at the pool, v_pages must equal
+ *                      k_pages + P*D (anything else is SPLASH_ERR_INVALID_ARGUMENT).
+ *                      Slot s of (page, h): k_pages[((page*Hkv + h)*2*P + s)*D + d],
+ *                      and the same offset from v_pages.
  *   k_scales, v_scales: fp32 [num_pages, Hkv, P]      one scale per (token, KV head)
  *   page_table       : int32 [num_seqs, max_pages_per_seq]; logical position j of
  *                      sequence b lives in page page_table[b][j / P], slot j % P.

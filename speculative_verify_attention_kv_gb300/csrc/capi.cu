@@ -93,6 +93,8 @@ int splash_kv_append(const float* k_new, const float* v_new, int num_new_tokens,
     return SPLASH_ERR_INVALID_ARGUMENT;
   if (page_size != kPageSize || !head_dim_ok(head_dim)) return SPLASH_ERR_UNSUPPORTED;
   if (num_new_tokens == 0 || num_seqs == 0) return SPLASH_OK;
+  if (k_pages && v_pages && v_pages != k_pages + (size_t)page_size * head_dim)
+    return SPLASH_ERR_INVALID_ARGUMENT;
   if (!k_new || !v_new || !k_pages || !v_pages || !k_scales || !v_scales || !page_table ||
       !context_lens || !block_lens)
     return SPLASH_ERR_INVALID_ARGUMENT;
@@ -114,6 +116,8 @@ int splash_kv_append_bf16(const uint16_t* k_new, const uint16_t* v_new, int num_
     return SPLASH_ERR_INVALID_ARGUMENT;
   if (page_size != kPageSize || !head_dim_ok(head_dim)) return SPLASH_ERR_UNSUPPORTED;
   if (num_new_tokens == 0 || num_seqs == 0) return SPLASH_OK;
+  if (k_pages && v_pages && v_pages != k_pages + (size_t)page_size * head_dim)
+    return SPLASH_ERR_INVALID_ARGUMENT;
   if (!k_new || !v_new || !k_pages || !v_pages || !k_scales || !v_scales || !page_table ||
       !context_lens || !block_lens)
     return SPLASH_ERR_INVALID_ARGUMENT;
@@ -189,6 +193,8 @@ static int verify_impl(
   if (path < 0 || path > 2 || ctas_per_class < 0 || num_pages < 0 || window < 0)
     return SPLASH_ERR_INVALID_ARGUMENT;
   if (num_q_tokens == 0 || num_seqs == 0) return SPLASH_OK;
+  if (k_pages && v_pages && v_pages != k_pages + (size_t)page_size * head_dim)
+    return SPLASH_ERR_INVALID_ARGUMENT;
   if (!q || !k_pages || !v_pages || !k_scales || !v_scales || !page_table || !context_lens ||
       !block_lens || !out || !lse || !workspace)
     return SPLASH_ERR_INVALID_ARGUMENT;

@@ -154,12 +154,13 @@ kv_append_kernel(const TIn* __restrict__ k_new, const TIn* __restrict__ v_new,
     }
     const int slot = pos % kPageSize;
     const size_t src = ((size_t)tok * num_kv_heads + h) * D + lane * EPL;
-    const size_t row = ((size_t)page * num_kv_heads + h) * kPageSize + slot;
+    const size_t row = ((size_t)page * num_kv_heads + h) * kPageSize + slot;   // scale index
+    const size_t code = code_offset(page, h, num_kv_heads, slot, D);
     float xk[EPL], xv[EPL];
     load_row<EPL>(k_new + src, xk);
     load_row<EPL>(v_new + src, xv);
-    quantise_store<EPL>(xk, k_pages + row * D + lane * EPL, k_scales + row, lane);
-    quantise_store<EPL>(xv, v_pages + row * D + lane * EPL, v_scales + row, lane);
+    quantise_store<EPL>(xk, k_pages + code + lane * EPL, k_scales + row, lane);
+    quantise_store<EPL>(xv, v_pages + code + lane * EPL, v_scales + row, lane);
   }
 }
 

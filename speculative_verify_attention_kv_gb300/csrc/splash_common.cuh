@@ -38,6 +38,15 @@ struct PlanHeader {
 };
 static_assert(sizeof(PlanHeader) == 64, "header size");
 
+// Code pool layout: one allocation [num_pages][Hkv][2][kPageSize][D] int8;
+// the (page, KV head) block holds the K codes of its 16 slots followed by
+// the V codes, so v_pages = k_pages + kPageSize * D and consecutive blocks are
+// 2 * kPageSize * D bytes apart (one 8 KB bulk copy stages both at D = 256).
+// Byte offset of slot `slot` of block (page, h) from k_pages (or v_pages):
+__host__ __device__ inline size_t code_offset(int page, int h, int num_kv_heads, int slot, int D) {
+  return (((size_t)page * num_kv_heads + h) * 2 * kPageSize + slot) * D;
+}
+
 // First key a unit (context ctx) needs: with a sliding window W > 0, verify
 // token t sees keys ctx + t - W < j <= ctx + t, so no row sees a key below
 // ctx - W + 1; tiles wholly below it are skipped and their pages never read.

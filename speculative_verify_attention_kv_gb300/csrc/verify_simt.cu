@@ -109,7 +109,7 @@ verify_simt_kernel(AttnParams p, int rows_cap) {
           const int page = ptab[j / kPageSize];
           if (page >= 0 && page < p.num_pages) {
             const int8_t* base = (which ? p.v_pages : p.k_pages) +
-                                 (((size_t)page * Hkv + h) * kPageSize + j % kPageSize) * D;
+                                 code_offset(page, h, Hkv, j % kPageSize, D);
             val = *reinterpret_cast<const uint4*>(base + c * 16);
           }
         }

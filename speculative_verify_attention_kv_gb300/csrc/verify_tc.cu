@@ -27,10 +27,12 @@
 //               (one thread issues at most one tcgen05.mma per ~120 cycles
 //               whatever N is; with A in TMEM, three issuing threads give
 //               nearly three times the rate of one)
-//   warp  15    producer: bulk async copies (TMA, untiled) of whole
-//               (page, KV head) blocks: codes into a 2-stage int8 staging
-//               ring ahead of the converters, scales straight into the
-//               3-stage scale arrays the softmax reads
+//   warp  15    producer: one bulk async copy (TMA, untiled) per (page, KV
+//               head) block, K and V codes together (8 KB at D = 256; the
+//               pool keeps them adjacent because a copy's issue cost is
+//               mostly per copy), into a 2-stage int8 staging ring ahead of
+//               the converters; scales straight into the 3-stage scale arrays
+//               the softmax reads
 // Buffers: fp16 K tiles x2 (free once QK of the tile is done), fp16 V tiles x3
 // (free once PV is done), so a slow stage does not stall the two behind it.
 // Handshakes are mbarriers; every wait gives up after ~1 s, sets
@@ -67,9 +69,8 @@ struct Cfg {
   static constexpr int kSCol = D / 2;                            // S[2]: 64 columns each
   static constexpr int kOCol = D / 2 + 2 * kTileKeys;            // O: D columns
   static_assert(kOCol + D <= (int)kTmemCols, "TMEM budget");
-  // staging ring stage: K codes [64][D], V codes [64][D]
-  static constexpr int kRingCodes = kTileKeys * D;
-  static constexpr int kRingStage = 2 * kRingCodes;
+  // staging ring stage: 4 (page, KV head) blocks of [K codes 16 x D][V codes 16 x D]
+  static constexpr int kRingStage = 2 * kTileKeys * D;
   // dynamic shared memory (offsets from a 1024-byte aligned base)
   static constexpr int kOffK = 0;                                        // fp16 K [2]
   static constexpr int kOffV = kOffK + kStages * kTileBytes;             // fp16 V [3]
@@ -307,8 +308,8 @@ struct SegIter {
 };
 
 struct Smem {
-  uint64_t ring_full[2][kRing];   // producer tx -> converters ([0] K codes, [1] V codes)
-  uint64_t ring_empty[2][kRing];  // converters -> producer
+  uint64_t ring_full[kRing];      // producer tx (K and V codes) -> converters
+  uint64_t ring_empty[2][kRing];  // converters done with a stage's [0] K / [1] V codes -> producer
   uint64_t sc_full[kVStages];     // producer cp.async (scales) -> softmax
   uint64_t sc_free[kVStages];     // softmax done with the scales -> producer
   uint64_t k_full[kStages];       // converters -> QK issuer (fp16 K of the tile ready)
@@ -372,16 +373,17 @@ struct PageWindow {
   }
 };
 
-// Producer (one warp): the K or the V codes of tile `it` of segment s into a
-// ring entry. The tile's 4 page ids come from the page window; lanes 0..3
-// each issue one bulk copy (the codes of one (page, KV head) block). Pages
-// past the sequence end or with an invalid id are skipped: their stale codes
-// are finite and the softmax gives their keys probability 0 without reading
-// their scales. Returns the page id of page (lane & 3), -1 if skipped.
+// Producer (one warp): the K and V codes of tile `it` of segment s into a
+// ring stage. The tile's 4 page ids come from the page window; lanes 0..3
+// each issue one bulk copy of a (page, KV head) block (K codes then V codes,
+// 2 x 16 x D bytes). Pages past the sequence end, below a sliding window or
+// with an invalid id are skipped: their stale codes are finite and the
+// softmax gives their keys probability 0 without reading their scales.
+// Returns the page id of page (lane & 3), -1 if skipped.
 template <int D>
 __device__ __forceinline__ int stage_codes(const AttnParams& p, const Seg& s, int it,
-                                           const int8_t* pool, uint8_t* dst, uint32_t bar,
-                                           int lane, PageWindow& win) {
+                                           uint8_t* dst, uint32_t bar, int lane,
+                                           PageWindow& win) {
   const int k0 = it * kTileKeys;
   const int npages = (s.Lk + kPageSize - 1) / kPageSize;
   int page = win.get(p, s.b, k0 / kPageSize, npages, lane);
@@ -391,12 +393,12 @@ __device__ __forceinline__ int stage_codes(const AttnParams& p, const Seg& s, in
   if (needed && page < 0 && lane < kPagesPerTile) report(p.device_status, SPLASH_DEVICE_BAD_PAGE);
   const int mask = (int)(__ballot_sync(0xffffffffu, page >= 0 && lane < kPagesPerTile) &
                          ((1u << kPagesPerTile) - 1));
-  constexpr uint32_t kBlock = kPageSize * D;          // codes of one (page, head)
+  constexpr uint32_t kBlock = 2 * kPageSize * D;      // K and V codes of one (page, head)
   if (lane == 0) mbar_expect_tx(bar, (uint32_t)__popc(mask) * kBlock);
   __syncwarp();
   if (lane < kPagesPerTile && page >= 0)
     bulk_g2s(smem_u32(dst) + lane * kBlock,
-             pool + ((size_t)page * p.num_kv_heads + s.h) * kBlock, kBlock, bar);
+             p.k_pages + code_offset(page, s.h, p.num_kv_heads, 0, D), kBlock, bar);
   return page;
 }
 
@@ -426,8 +428,10 @@ __host__ __device__ constexpr int tile_row_of_key(int n) {
   return 8 * ((n % 16) / 2) + 2 * (n / 16) + (n % 2);
 }
 
+// src: the K (or V) codes of page 0 of a ring stage, pages 2 x 16 x D bytes apart
 template <int D>
 __device__ __forceinline__ void convert_codes(const uint8_t* src, uint8_t* dst, int lt) {
+  constexpr int kPageStride = 2 * kPageSize * D;
   // units of 16 codes (one 16-byte load, two 16-byte fp16 stores); a warp
   // covers two key rows, and the 128B swizzle keeps its stores conflict-free
   constexpr int kUnits = kTileKeys * D / 16;
@@ -437,7 +441,9 @@ __device__ __forceinline__ void convert_codes(const uint8_t* src, uint8_t* dst, 
 #pragma unroll
   for (int q = 0; q < kPer; ++q) {
     const int u = q * kLoadThreads + lt;
-    w[q] = *reinterpret_cast<const uint4*>(src + (u / (D / 16)) * D + (u % (D / 16)) * 16);
+    const int key = u / (D / 16);
+    w[q] = *reinterpret_cast<const uint4*>(src + (key / kPageSize) * kPageStride +
+                                           (key % kPageSize) * D + (u % (D / 16)) * 16);
   }
 #pragma unroll
   for (int q = 0; q < kPer; ++q) {
@@ -493,11 +499,10 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
   float* lse_part = reinterpret_cast<float*>(p.ws + L.lse_part);
 
   if (tid == 0) {
-    for (int s = 0; s < kRing; ++s)
-      for (int kv = 0; kv < 2; ++kv) {
-        mbar_init(smem_u32(&sh->ring_full[kv][s]), 1);
-        mbar_init(smem_u32(&sh->ring_empty[kv][s]), kLoadThreads);
-      }
+    for (int s = 0; s < kRing; ++s) {
+      mbar_init(smem_u32(&sh->ring_full[s]), 1);
+      for (int kv = 0; kv < 2; ++kv) mbar_init(smem_u32(&sh->ring_empty[kv][s]), kLoadThreads);
+    }
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&sh->k_full[s]), kLoadThreads);
       mbar_init(smem_u32(&sh->k_free[s]), 1);
@@ -813,7 +818,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
         const uint32_t ph = (g / kRing) & 1;
         const uint8_t* stage = ring + r * C::kRingStage;
         // K codes -> fp16 K tile; the QK of the tile may start at once
-        ok = sync.wait(smem_u32(&sh->ring_full[0][r]), ph) &&
+        ok = sync.wait(smem_u32(&sh->ring_full[r]), ph) &&
              sync.wait(smem_u32(&sh->k_free[st]), ((g / kStages) & 1) ^ 1);
         if (!ok) break;
         convert_codes<D>(stage, kbuf + st * C::kTileBytes, lt);
@@ -821,10 +826,9 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
         fence_async_smem();
         mbar_arrive(smem_u32(&sh->k_full[st]));
         // V codes -> fp16 V tile
-        ok = sync.wait(smem_u32(&sh->ring_full[1][r]), ph) &&
-             sync.wait(smem_u32(&sh->v_free[vst]), ((g / kVStages) & 1) ^ 1);
+        ok = sync.wait(smem_u32(&sh->v_free[vst]), ((g / kVStages) & 1) ^ 1);
         if (!ok) break;
-        convert_codes<D>(stage + C::kRingCodes, vbuf + vst * C::kTileBytes, lt);
+        convert_codes<D>(stage + kPageSize * D, vbuf + vst * C::kTileBytes, lt);
         mbar_arrive(smem_u32(&sh->ring_empty[1][r]));
         fence_async_smem();
         mbar_arrive(smem_u32(&sh->v_full[vst]));
@@ -841,21 +845,15 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
         const int r = g % kRing, vst = g % kVStages;
         const uint32_t ph = ((g / kRing) & 1) ^ 1;
         uint8_t* stage = ring + r * C::kRingStage;
-        // K codes once the converters are done with the K codes of tile g - 2
-        if (lane == 0) ok = sync.wait(smem_u32(&sh->ring_empty[0][r]), ph);
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) break;
-        const int page = stage_codes<D>(p, s, it, p.k_pages, stage, smem_u32(&sh->ring_full[0][r]),
-                                        lane, win);
-        // V codes and the scales once the converters are done with the V codes
-        // of tile g - 2 and the softmax with the scales of tile g - 3
+        // codes once the converters are done with tile g - 2's K and V codes,
+        // scales once the softmax is done with the scales of tile g - 3
         if (lane == 0)
-          ok = sync.wait(smem_u32(&sh->ring_empty[1][r]), ph) &&
+          ok = sync.wait(smem_u32(&sh->ring_empty[0][r]), ph) &&
+               sync.wait(smem_u32(&sh->ring_empty[1][r]), ph) &&
                sync.wait(smem_u32(&sh->sc_free[vst]), ((g / kVStages) & 1) ^ 1);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
-        stage_codes<D>(p, s, it, p.v_pages, stage + C::kRingCodes, smem_u32(&sh->ring_full[1][r]),
-                       lane, win);
+        const int page = stage_codes<D>(p, s, it, stage, smem_u32(&sh->ring_full[r]), lane, win);
         stage_scales(p, s, page, scales + vst * 2 * kTileKeys, smem_u32(&sh->sc_full[vst]), lane);
       }
     }

@@ -103,13 +103,30 @@ def _stream(stream) -> ctypes.c_void_p:
 
 
 def alloc_pool(num_pages: int, num_kv_heads: int, head_dim: int, device="cuda"):
-    """Zeroed paged pool: (k_pages, v_pages, k_scales, v_scales) in the library's layout."""
-    codes = (num_pages, num_kv_heads, PAGE_SIZE, head_dim)
+    """Zeroed paged pool in the library's layout: (k_pages, v_pages, k_scales,
+    v_scales). The codes are one allocation [num_pages, Hkv, 2, P, D]; k_pages
+    and v_pages are its [:, :, 0] and [:, :, 1] views ([num_pages, Hkv, P, D]
+    each, K and V codes of a (page, KV head) adjacent)."""
+    codes = torch.zeros((num_pages, num_kv_heads, 2, PAGE_SIZE, head_dim), dtype=torch.int8,
+                        device=device)
     scales = (num_pages, num_kv_heads, PAGE_SIZE)
-    return (torch.zeros(codes, dtype=torch.int8, device=device),
-            torch.zeros(codes, dtype=torch.int8, device=device),
+    return (codes[:, :, 0], codes[:, :, 1],
             torch.zeros(scales, dtype=torch.float32, device=device),
             torch.zeros(scales, dtype=torch.float32, device=device))
+
+
+def _check_pool(k_pages, v_pages):
+    """k_pages / v_pages: the two halves of one [num_pages, Hkv, 2, P, D] code pool."""
+    for n, t in (("k_pages", k_pages), ("v_pages", v_pages)):
+        if not isinstance(t, torch.Tensor) or t.dtype != torch.int8 or not t.is_cuda or t.dim() != 4:
+            raise TypeError(f"{n} must be a 4-D int8 CUDA tensor")
+    num_pages, hkv, P, D = k_pages.shape
+    want = (hkv * 2 * P * D, 2 * P * D, D, 1)
+    if tuple(v_pages.shape) != tuple(k_pages.shape) or tuple(k_pages.stride()) != want \
+            or tuple(v_pages.stride()) != want \
+            or v_pages.data_ptr() != k_pages.data_ptr() + P * D:
+        raise ValueError("k_pages / v_pages must be the [:, :, 0] / [:, :, 1] views of one "
+                         "[num_pages, Hkv, 2, P, D] pool (see alloc_pool)")
 
 
 def splash_kv_append(k_new, v_new, k_pages, v_pages, k_scales, v_scales, page_table,
@@ -119,8 +136,7 @@ def splash_kv_append(k_new, v_new, k_pages, v_pages, k_scales, v_scales, page_ta
         raise TypeError("k_new must be float32 or bfloat16")
     _check(k_new, "k_new", k_new.dtype, 3)
     _check(v_new, "v_new", k_new.dtype, 3)
-    for n, t in (("k_pages", k_pages), ("v_pages", v_pages)):
-        _check(t, n, torch.int8, 4)
+    _check_pool(k_pages, v_pages)
     for n, t in (("k_scales", k_scales), ("v_scales", v_scales)):
         _check(t, n, torch.float32, 3)
     _check(page_table, "page_table", torch.int32, 2)
@@ -190,8 +206,7 @@ def splash_verify_attention(q, k_pages, v_pages, k_scales, v_scales, page_table,
     _check(q, "q", torch.bfloat16, 3)
     _check(out, "out", torch.bfloat16, 3)
     _check(lse, "lse", torch.float32, 2)
-    for n, t in (("k_pages", k_pages), ("v_pages", v_pages)):
-        _check(t, n, torch.int8, 4)
+    _check_pool(k_pages, v_pages)
     for n, t in (("k_scales", k_scales), ("v_scales", v_scales)):
         _check(t, n, torch.float32, 3)
     _check(page_table, "page_table", torch.int32, 2)
@@ -234,8 +249,7 @@ def splash_verify_attention_fixed_scratch(q, k_pages, v_pages, k_scales, v_scale
     _check(q, "q", torch.bfloat16, 3)
     _check(out, "out", torch.bfloat16, 3)
     _check(lse, "lse", torch.float32, 2)
-    for n, t in (("k_pages", k_pages), ("v_pages", v_pages)):
-        _check(t, n, torch.int8, 4)
+    _check_pool(k_pages, v_pages)
     for n, t in (("k_scales", k_scales), ("v_scales", v_scales)):
         _check(t, n, torch.float32, 3)
     _check(page_table, "page_table", torch.int32, 2)

@@ -52,10 +52,11 @@ def test_status_strings(sk):
 
 
 FAKE = ctypes.c_void_p(256)  # never dereferenced: validation fails first
+FAKE_V = ctypes.c_void_p(256 + 16 * 128)   # V half of the code pool at D = 128: K + P*D
 
 
 def _append(sk, **kw):
-    a = dict(k=FAKE, v=FAKE, n=4, kp=FAKE, vp=FAKE, ks=FAKE, vs=FAKE, tab=FAKE, maxp=4,
+    a = dict(k=FAKE, v=FAKE, n=4, kp=FAKE, vp=FAKE_V, ks=FAKE, vs=FAKE, tab=FAKE, maxp=4,
              ctx=FAKE, T=FAKE, B=1, hkv=2, D=128, P=16, pages=8, st=None, stream=None)
     a.update(kw)
     return sk.LIB.splash_kv_append(a["k"], a["v"], a["n"], a["kp"], a["vp"], a["ks"], a["vs"],
@@ -67,13 +68,14 @@ def _append(sk, **kw):
     (dict(P=8), -2), (dict(D=96), -2), (dict(D=512), -2), (dict(hkv=0), -1), (dict(n=-1), -1),
     (dict(B=-2), -1), (dict(maxp=0), -1), (dict(k=None), -1), (dict(tab=None), -1),
     (dict(vs=None), -1), (dict(n=0), 0), (dict(B=0), 0),
+    (dict(vp=FAKE), -1),              # V codes not at K + P*D of one pool
 ])
 def test_kv_append_argument_errors(sk, kw, code):
     assert _append(sk, **kw) == code
 
 
 def _attn(sk, **kw):
-    a = dict(q=FAKE, n=4, kp=FAKE, vp=FAKE, ks=FAKE, vs=FAKE, tab=FAKE, maxp=4, ctx=FAKE,
+    a = dict(q=FAKE, n=4, kp=FAKE, vp=FAKE_V, ks=FAKE, vs=FAKE, tab=FAKE, maxp=4, ctx=FAKE,
              T=FAKE, B=1, hq=8, hkv=2, D=128, P=16, pages=8, maxT=4, sm=0.088, out=FAKE,
              lse=FAKE, ws=FAKE, wsb=1 << 30, st=None, stream=None, path=0, ctas=0)
     a.update(kw)
@@ -90,6 +92,7 @@ def _attn(sk, **kw):
     (dict(ctas=-1), -1), (dict(q=None), -1), (dict(ws=None), -1), (dict(lse=None), -1),
     (dict(ws=ctypes.c_void_p(256 + 16)), -1),   # workspace not 256-byte aligned
     (dict(n=0), 0), (dict(B=0), 0),
+    (dict(vp=FAKE), -1),              # V codes not at K + P*D of one pool
 ])
 def test_verify_attention_argument_errors(sk, kw, code):
     assert _attn(sk, **kw) == code

@@ -268,11 +268,9 @@ def test_deterministic_and_page_permutation_bitwise(path):
     o2, l2 = [t.clone() for t in r.attend(path=path)]
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
     perm = torch.from_numpy(np.random.default_rng(3).permutation(W.num_pages)).cuda().long()
-    newpool = []
-    for t in r.pool:
-        n = torch.empty_like(t)
+    newpool = sk.alloc_pool(W.num_pages, W.spec.num_kv_heads, W.spec.head_dim)
+    for n, t in zip(newpool, r.pool):
         n[perm] = t
-        newpool.append(n)
     r.pool = tuple(newpool)
     tab = r.table.long()
     r.table = torch.where(tab >= 0, perm[tab.clamp(min=0)], tab).int().contiguous()
