@@ -79,7 +79,7 @@ plan_kernel(const int32_t* __restrict__ context_lens, const int32_t* __restrict_
         const int rows = T * group;
         cls = path == 1 ? kClassSimt : path == 2 ? kClassTensor
                         : (rows >= kTensorMinRows ? kClassTensor : kClassSimt);
-        tiles = unit_tiles(ctx, T, window, tile[cls]);
+        tiles = unit_tiles(ctx, T, window, cls == 0 ? tile[0] : tile[1]);
       }
       seq_T[b] = T;
       seq_ctx[b] = ctx;
@@ -128,10 +128,13 @@ plan_kernel(const int32_t* __restrict__ context_lens, const int32_t* __restrict_
       int ns = 0, cf = 0;
       if (cls >= 0) {
         const int T = seq_T[b], ctx = seq_ctx[b];
-        const int tiles = unit_tiles(ctx, T, window, tile[cls]);
+        const int tk = cls == 0 ? tile[0] : tile[1];        // selects, not a local-memory index
+        const int tot = cls == 0 ? total[0] : total[1];
+        const int nce = cls == 0 ? ncta_eff[0] : ncta_eff[1];
+        const int tiles = unit_tiles(ctx, T, window, tk);
         const int tp = stp[cls * (num_seqs + 1) + b] + h * tiles;
-        cf = cta_of_tile(tp, total[cls], ncta_eff[cls]);
-        const int cl = cta_of_tile(tp + tiles - 1, total[cls], ncta_eff[cls]);
+        cf = cta_of_tile(tp, tot, nce);
+        const int cl = cta_of_tile(tp + tiles - 1, tot, nce);
         ns = cl - cf + 1;
         if (ns > 1) rows = ns * T * group;
       }
@@ -187,25 +190,43 @@ lse_combine_kernel(int num_q_tokens, int num_q_heads, int num_seqs, int num_kv_h
   const int r = (i - q_off[b]) * group + g;
   const long long base = part_base[u];
 
+  // lse_i of the splits, 32 at a time across the lanes
   float m = -INFINITY;
   for (int j = lane; j < n; j += 32) m = fmaxf(m, lse_part[base + (long long)j * R + r]);
   m = warp_max(m);
+  float wsum = 0.f;
+  for (int j = lane; j < n; j += 32) {
+    const float lj = lse_part[base + (long long)j * R + r];
+    wsum += (lj == -INFINITY) ? 0.f : __expf(lj - m);
+  }
+  wsum = warp_sum(wsum);
+  // O: the partial rows of four splits are loaded before any is accumulated
   float acc[EPL];
 #pragma unroll
   for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
-  float wsum = 0.f;
-  for (int j = 0; j < n; ++j) {
-    const long long pr = base + (long long)j * R + r;
-    const float lj = lse_part[pr];
-    const float w = (lj == -INFINITY) ? 0.f : __expf(lj - m);
-    wsum += w;
-    if (w != 0.f) {
-      const float* src = o_part + pr * D + lane * EPL;
+  for (int j0 = 0; j0 < n; j0 += 4) {
+    float w[4];
+    float2 v[4][EPL / 2];
 #pragma unroll
-      for (int e = 0; e < EPL; e += 2) {
-        const float2 v = *reinterpret_cast<const float2*>(src + e);
-        acc[e] = fmaf(w, v.x, acc[e]);
-        acc[e + 1] = fmaf(w, v.y, acc[e + 1]);
+    for (int k = 0; k < 4; ++k) {
+      const int j = j0 + k;
+      w[k] = 0.f;
+      if (j < n) {
+        const long long pr = base + (long long)j * R + r;
+        const float lj = lse_part[pr];
+        w[k] = (lj == -INFINITY) ? 0.f : __expf(lj - m);
+        const float* src = o_part + pr * D + lane * EPL;
+#pragma unroll
+        for (int e = 0; e < EPL / 2; ++e) v[k][e] = *reinterpret_cast<const float2*>(src + 2 * e);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      if (w[k] == 0.f) continue;
+#pragma unroll
+      for (int e = 0; e < EPL / 2; ++e) {
+        acc[2 * e] = fmaf(w[k], v[k][e].x, acc[2 * e]);
+        acc[2 * e + 1] = fmaf(w[k], v[k][e].y, acc[2 * e + 1]);
       }
     }
   }

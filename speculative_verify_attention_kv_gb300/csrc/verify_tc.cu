@@ -30,11 +30,13 @@
 //   warp  15    producer: one bulk async copy (TMA, untiled) per (page, KV
 //               head) block, K and V codes together (8 KB at D = 256; the
 //               pool keeps them adjacent because a copy's issue cost is
-//               mostly per copy), into a 2-stage int8 staging ring ahead of
+//               mostly per copy), into a 3-stage int8 staging ring ahead of
 //               the converters; scales straight into the 3-stage scale arrays
 //               the softmax reads
-// Buffers: fp16 K tiles x2 (free once QK of the tile is done), fp16 V tiles x3
-// (free once PV is done), so a slow stage does not stall the two behind it.
+// Buffers (shared memory): int8 staging ring x3, fp16 K tiles x2 (free once
+// QK of the tile is done), fp16 V tiles x2 (free once PV is done), scales x3.
+// A third staging stage bought with a V tile measured 5% faster: the copies'
+// latency, not the PV chain, limited the loop.
 // Handshakes are mbarriers; every wait gives up after ~1 s, sets
 // SPLASH_DEVICE_TIMEOUT and lets the CTA drain and free its TMEM.
 #include "splash_common.cuh"
@@ -45,8 +47,9 @@ namespace tc {
 constexpr int kTileKeys = 64;
 constexpr int kPagesPerTile = kTileKeys / kPageSize;
 constexpr int kStages = 2;                    // S/P buffers in TMEM, fp16 K tiles
-constexpr int kVStages = 3;                   // fp16 V tiles and the scale arrays
-constexpr int kRing = 2;                      // int8 staging stages
+constexpr int kVStages = 2;                   // fp16 V tiles
+constexpr int kScStages = 3;                  // K/V scale arrays
+constexpr int kRing = 3;                      // int8 staging stages
 constexpr int kSoftmaxWarps = 8;              // 2 per TMEM lane quarter, 16 rows each
 constexpr int kLoadWarps = 4;
 constexpr int kLoadThreads = 32 * kLoadWarps;
@@ -72,11 +75,11 @@ struct Cfg {
   // staging ring stage: 4 (page, KV head) blocks of [K codes 16 x D][V codes 16 x D]
   static constexpr int kRingStage = 2 * kTileKeys * D;
   // dynamic shared memory (offsets from a 1024-byte aligned base)
-  static constexpr int kOffK = 0;                                        // fp16 K [2]
-  static constexpr int kOffV = kOffK + kStages * kTileBytes;             // fp16 V [3]
-  static constexpr int kOffRing = kOffV + kVStages * kTileBytes;         // int8 [2]
-  static constexpr int kOffScales = kOffRing + kRing * kRingStage;       // fp32 [3][2][64]
-  static constexpr int kOffBars = kOffScales + kVStages * 2 * kTileKeys * 4;
+  static constexpr int kOffK = 0;                                        // fp16 K [kStages]
+  static constexpr int kOffV = kOffK + kStages * kTileBytes;             // fp16 V [kVStages]
+  static constexpr int kOffRing = kOffV + kVStages * kTileBytes;         // int8 [kRing]
+  static constexpr int kOffScales = kOffRing + kRing * kRingStage;       // fp32 [kScStages][2][64]
+  static constexpr int kOffBars = kOffScales + kScStages * 2 * kTileKeys * 4;
   static constexpr int kBarBytes = 512;
   static constexpr int kSmemUsed = kOffBars + kBarBytes;
   // + up to 1 KB to align the base (the kernel checks the room it got); at
@@ -310,8 +313,8 @@ struct SegIter {
 struct Smem {
   uint64_t ring_full[kRing];      // producer tx (K and V codes) -> converters
   uint64_t ring_empty[2][kRing];  // converters done with a stage's [0] K / [1] V codes -> producer
-  uint64_t sc_full[kVStages];     // producer cp.async (scales) -> softmax
-  uint64_t sc_free[kVStages];     // softmax done with the scales -> producer
+  uint64_t sc_full[kScStages];    // producer cp.async (scales) -> softmax
+  uint64_t sc_free[kScStages];    // softmax done with the scales -> producer
   uint64_t k_full[kStages];       // converters -> QK issuer (fp16 K of the tile ready)
   uint64_t v_full[kVStages];      // converters -> PV issuer (fp16 V of the tile ready)
   uint64_t k_free[kStages];       // QK done -> converters
@@ -510,9 +513,11 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
       mbar_init(smem_u32(&sh->p_full[s]), 32 * kSoftmaxWarps);
       mbar_init(smem_u32(&sh->p_free[s]), 1);
     }
-    for (int s = 0; s < kVStages; ++s) {
+    for (int s = 0; s < kScStages; ++s) {
       mbar_init(smem_u32(&sh->sc_full[s]), 32);     // one cp.async arrival per producer lane
       mbar_init(smem_u32(&sh->sc_free[s]), 32 * kSoftmaxWarps);
+    }
+    for (int s = 0; s < kVStages; ++s) {
       mbar_init(smem_u32(&sh->v_free[s]), 1);
       mbar_init(smem_u32(&sh->v_full[s]), kLoadThreads);
     }
@@ -624,8 +629,8 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
 
       float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};   // l: this thread's columns
       for (int it = s.i0; it < s.i1 && ok; ++it, ++g) {
-        const int st = g % kStages, vst = g % kVStages;
-        ok = sync.wait(smem_u32(&sh->sc_full[vst]), (g / kVStages) & 1) &&
+        const int st = g % kStages, sst = g % kScStages;
+        ok = sync.wait(smem_u32(&sh->sc_full[sst]), (g / kScStages) & 1) &&
              sync.wait(smem_u32(&sh->s_full[st]), (g / kStages) & 1);
         if (!ok) break;
         fence_after();
@@ -633,7 +638,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
         float alpha[2] = {1.f, 1.f};
         if (warp_live) {
           const int k0 = it * kTileKeys;
-          const float* ks = scales + vst * 2 * kTileKeys;
+          const float* ks = scales + sst * 2 * kTileKeys;
           const float* vs = ks + kTileKeys;
           uint32_t sv[32];
           tmem_ld16x256_x8(tmem + lane_base + C::kSCol + st * kTileKeys, sv);
@@ -747,7 +752,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
             tmem_st16x256_x8(tmem + lane_base + C::kOCol + c0, v);
           }
         }
-        mbar_arrive(smem_u32(&sh->sc_free[vst]));          // scales of this tile are read
+        mbar_arrive(smem_u32(&sh->sc_free[sst]));          // scales of this tile are read
         if (warp_live) {
           tmem_st16x128_x8(tmem + lane_base + C::kSCol + st * kTileKeys, pw);
           tmem_wait_st();
@@ -842,7 +847,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
     PageWindow win;
     while (ok && iter.next(s)) {
       for (int it = s.i0; it < s.i1; ++it, ++g) {
-        const int r = g % kRing, vst = g % kVStages;
+        const int r = g % kRing, sst = g % kScStages;
         const uint32_t ph = ((g / kRing) & 1) ^ 1;
         uint8_t* stage = ring + r * C::kRingStage;
         // codes once the converters are done with tile g - 2's K and V codes,
@@ -850,11 +855,11 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
         if (lane == 0)
           ok = sync.wait(smem_u32(&sh->ring_empty[0][r]), ph) &&
                sync.wait(smem_u32(&sh->ring_empty[1][r]), ph) &&
-               sync.wait(smem_u32(&sh->sc_free[vst]), ((g / kVStages) & 1) ^ 1);
+               sync.wait(smem_u32(&sh->sc_free[sst]), ((g / kScStages) & 1) ^ 1);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
         const int page = stage_codes<D>(p, s, it, stage, smem_u32(&sh->ring_full[r]), lane, win);
-        stage_scales(p, s, page, scales + vst * 2 * kTileKeys, smem_u32(&sh->sc_full[vst]), lane);
+        stage_scales(p, s, page, scales + sst * 2 * kTileKeys, smem_u32(&sh->sc_full[sst]), lane);
       }
     }
   } else {
