@@ -642,10 +642,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
           const float* vs = ks + kTileKeys;
           uint32_t sv[32];
           tmem_ld16x256_x8(tmem + lane_base + C::kSCol + st * kTileKeys, sv);
-          tmem_wait_ld();
-          // x = S * sK (packed fp32x2); masked columns -> -inf (their scales
-          // are not read: pages past the end may hold anything)
-          // this thread's keys: 16*quad + 2i + {0,1} (see tile_row_of_key)
+          // the K scales load while the TMEM load is in flight
           float2 ks2[8], x[2][8];
 #pragma unroll
           for (int i4 = 0; i4 < 4; ++i4) {
@@ -653,6 +650,10 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
             ks2[2 * i4] = make_float2(kq.x, kq.y);
             ks2[2 * i4 + 1] = make_float2(kq.z, kq.w);
           }
+          tmem_wait_ld();
+          // x = S * sK (packed fp32x2); masked columns -> -inf (their scales
+          // are not read: pages past the end may hold anything)
+          // this thread's keys: 16*quad + 2i + {0,1} (see tile_row_of_key)
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
 #pragma unroll
