@@ -431,32 +431,41 @@ __host__ __device__ constexpr int tile_row_of_key(int n) {
   return 8 * ((n % 16) / 2) + 2 * (n / 16) + (n % 2);
 }
 
-// src: the K (or V) codes of page 0 of a ring stage, pages 2 x 16 x D bytes apart
+// src: the K (or V) codes of page 0 of a ring stage, pages 2 x 16 x D bytes apart.
+// Units of 16 codes: one 16-byte shared load, two 16-byte fp16 stores into the
+// 128B-swizzled tile (row tile_row_of_key(key), 16-byte chunks 2c and 2c + 1
+// of the row's 64-column atom c / 4). 16-byte accesses are served per quarter
+// warp, so each quarter takes 4 chunks of an even key row and 4 of the next
+// key's row (tile rows n, n + 1): its 8 loads and each of its two stores fall
+// in 8 distinct bank groups.
 template <int D>
 __device__ __forceinline__ void convert_codes(const uint8_t* src, uint8_t* dst, int lt) {
   constexpr int kPageStride = 2 * kPageSize * D;
-  // units of 16 codes (one 16-byte load, two 16-byte fp16 stores); a warp
-  // covers two key rows, and the 128B swizzle keeps its stores conflict-free
-  constexpr int kUnits = kTileKeys * D / 16;
-  constexpr int kPer = kUnits / kLoadThreads;
-  static_assert(kUnits % kLoadThreads == 0, "converter units");
-  uint4 w[kPer];
+  constexpr int kChunks = D / 16;                     // 16-code chunks per key row
+  constexpr int kQuartersPerPair = kChunks / 4;       // quarter warps per two key rows
+  constexpr int kKeysPerPass = kLoadThreads * 16 / D;
+  constexpr int kPer = kTileKeys / kKeysPerPass;
+  static_assert(kChunks % 4 == 0 && kTileKeys % kKeysPerPass == 0, "converter units");
+  const int w = lt >> 5, l = lt & 31, qtr = l >> 3, rsel = (l >> 2) & 1, j = l & 3;
+  const int pair = qtr / kQuartersPerPair, qq = qtr % kQuartersPerPair;
+  const int c16 = 8 * (qq >> 1) + 4 * (rsel ^ (qq & 1)) + j;
+  const int key_in_pass = w * (32 * 16 / D) + 2 * pair + rsel;
+  uint4 wv[kPer];
 #pragma unroll
   for (int q = 0; q < kPer; ++q) {
-    const int u = q * kLoadThreads + lt;
-    const int key = u / (D / 16);
-    w[q] = *reinterpret_cast<const uint4*>(src + (key / kPageSize) * kPageStride +
-                                           (key % kPageSize) * D + (u % (D / 16)) * 16);
+    const int key = q * kKeysPerPass + key_in_pass;
+    wv[q] = *reinterpret_cast<const uint4*>(src + (key / kPageSize) * kPageStride +
+                                            (key % kPageSize) * D + c16 * 16);
   }
 #pragma unroll
   for (int q = 0; q < kPer; ++q) {
-    const int u = q * kLoadThreads + lt;
-    const int n = tile_row_of_key(u / (D / 16)), c8 = 2 * (u % (D / 16));
+    const int key = q * kKeysPerPass + key_in_pass;
+    const int n = tile_row_of_key(key), c8 = 2 * c16;
     uint4 h0, h1;
-    i8x4_to_h2x2(w[q].x, h0.x, h0.y);
-    i8x4_to_h2x2(w[q].y, h0.z, h0.w);
-    i8x4_to_h2x2(w[q].z, h1.x, h1.y);
-    i8x4_to_h2x2(w[q].w, h1.z, h1.w);
+    i8x4_to_h2x2(wv[q].x, h0.x, h0.y);
+    i8x4_to_h2x2(wv[q].y, h0.z, h0.w);
+    i8x4_to_h2x2(wv[q].z, h1.x, h1.y);
+    i8x4_to_h2x2(wv[q].w, h1.z, h1.w);
     const uint32_t row = (c8 / 8) * (kTileKeys * 128) + n * 128;
     *reinterpret_cast<uint4*>(dst + row + (((c8 & 7) ^ (n & 7)) << 4)) = h0;
     *reinterpret_cast<uint4*>(dst + row + ((((c8 + 1) & 7) ^ (n & 7)) << 4)) = h1;
