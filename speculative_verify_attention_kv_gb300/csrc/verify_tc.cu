@@ -415,8 +415,10 @@ __device__ __forceinline__ void stage_scales(const AttnParams& p, const Seg& s, 
   if (ps >= 0) {
     const float* src = (lane < 16 ? p.k_scales : p.v_scales) +
                        ((size_t)ps * p.num_kv_heads + s.h) * kPageSize + 4 * (lane & 3);
+    // page sj's 16-byte chunk c sits at chunk c ^ sj of the page's 64 bytes, so
+    // the softmax's four lanes reading chunk c of pages 0..3 hit distinct banks
     const uint32_t dst = smem_u32(scales) + (lane < 16 ? 0 : kTileKeys * 4) +
-                         (sj * kPageSize + 4 * (lane & 3)) * 4;
+                         (sj * kPageSize + 4 * ((lane & 3) ^ sj)) * 4;
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
   }
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(scale_bar)
@@ -655,7 +657,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
           float2 ks2[8], x[2][8];
 #pragma unroll
           for (int i4 = 0; i4 < 4; ++i4) {
-            const float4 kq = *reinterpret_cast<const float4*>(ks + 16 * quad + 4 * i4);
+            const float4 kq = *reinterpret_cast<const float4*>(ks + 16 * quad + 4 * (i4 ^ quad));
             ks2[2 * i4] = make_float2(kq.x, kq.y);
             ks2[2 * i4 + 1] = make_float2(kq.z, kq.w);
           }
@@ -711,7 +713,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
           float2 vs2[8];
 #pragma unroll
           for (int i4 = 0; i4 < 4; ++i4) {
-            const float4 vq4 = *reinterpret_cast<const float4*>(vs + 16 * quad + 4 * i4);
+            const float4 vq4 = *reinterpret_cast<const float4*>(vs + 16 * quad + 4 * (i4 ^ quad));
             vs2[2 * i4] = make_float2(vq4.x, vq4.y);
             vs2[2 * i4 + 1] = make_float2(vq4.z, vq4.w);
           }
