@@ -103,3 +103,33 @@ def test_workspace_query_rejects_bad_shapes(sk):
     assert f(1, 4, 7, 2, 128, 4) == 0
     assert f(1, 4, 8, 2, 100, 4) == 0
     assert f(1, 4, 8, 2, 128, 64) == 0
+
+
+def _accept(sk, **kw):
+    a = dict(x=FAKE, y=FAKE, n=8, T=FAKE, ctx=FAKE, acc=FAKE, nxt=FAKE, B=2, st=None, stream=None)
+    a.update(kw)
+    return sk.LIB.splash_accept_commit(a["x"], a["y"], a["n"], a["T"], a["ctx"], a["acc"],
+                                       a["nxt"], a["B"], a["st"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(n=-1), -1), (dict(B=-1), -1), (dict(T=None), -1), (dict(ctx=None), -1),
+    (dict(acc=None), -1), (dict(nxt=None), -1), (dict(x=None), -1), (dict(y=None), -1),
+    (dict(B=0), 0),                   # nothing to do
+])
+def test_accept_commit_argument_errors(sk, kw, code):
+    assert _accept(sk, **kw) == code
+
+
+def test_sliding_window_argument_errors(sk):
+    a = dict(q=FAKE, n=4, kp=FAKE, vp=FAKE_V, ks=FAKE, vs=FAKE, tab=FAKE, maxp=4, ctx=FAKE,
+             T=FAKE, B=1, hq=8, hkv=2, D=128, P=16, pages=8, maxT=4, sm=0.088)
+    args = [a[k] for k in ("q", "n", "kp", "vp", "ks", "vs", "tab", "maxp", "ctx", "T", "B", "hq",
+                           "hkv", "D", "P", "pages", "maxT", "sm")]
+    tail = [FAKE, FAKE, FAKE, 1 << 30, None, None, 0, 0]
+    f = sk.LIB.splash_verify_attention_swa
+    assert f(*args, -1, *tail) == -1                      # negative window
+    assert f(*args, 5, FAKE, FAKE, FAKE, 1 << 30, None, None, 3, 0) == -1   # bad path
+    args_bad_pool = list(args)
+    args_bad_pool[3] = FAKE                                # V codes not at K + P*D
+    assert f(*args_bad_pool, 5, *tail) == -1
