@@ -84,7 +84,8 @@ enum {
 /* Human-readable name of a SPLASH_* status (static string, never NULL). */
 const char* splash_status_string(int status);
 
-/* Library ABI version (increments on any signature change). */
+/* Library ABI version (increments on any signature or layout change; 2 = the
+ * interleaved K/V code pool). */
 int splash_abi_version(void);
 
 /* 1 if the tensor-core attention kernel is built for this head_dim, else 0

@@ -77,7 +77,8 @@ const char* splash_status_string(int status) {
   return "SPLASH_UNKNOWN_STATUS";
 }
 
-int splash_abi_version(void) { return 1; }
+// 2: one interleaved K/V code pool (v_pages = k_pages + P * D)
+int splash_abi_version(void) { return 2; }
 
 int splash_tensor_path_supported(int head_dim) {
   return head_dim_ok(head_dim) && tc_supported(head_dim) ? 1 : 0;

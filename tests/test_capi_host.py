@@ -48,7 +48,7 @@ def test_status_strings(sk):
     assert sk.status_string(-3) == "SPLASH_ERR_WORKSPACE_TOO_SMALL"
     assert sk.status_string(-4) == "SPLASH_ERR_CUDA"
     assert sk.status_string(12345) == "SPLASH_UNKNOWN_STATUS"
-    assert sk.LIB.splash_abi_version() == 1
+    assert sk.LIB.splash_abi_version() == 2
 
 
 FAKE = ctypes.c_void_p(256)  # never dereferenced: validation fails first
