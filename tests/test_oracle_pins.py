@@ -474,3 +474,36 @@ def test_accept_commit_bounds_and_full_acceptance():
     acc2, _, nxt2 = O.accept_commit(x2, y2, T, np.zeros(50, np.int32))
     assert np.array_equal(acc2, np.maximum(T - 1, 0))
     assert np.all(nxt2[T > 0] == 99)
+
+
+def test_planted_accept_off_by_one_is_caught(monkeypatch):
+    # compares draft x_{i+1} with the target's choice after x_{i+1} (y_{i+1}) instead of y_i
+    def wrong(block_tokens, target_tokens, block_lens, context_lens):
+        acc, ctx, nxt = [], [], []
+        off = 0
+        for b, T in enumerate(block_lens):
+            T = int(T)
+            x, y = list(block_tokens[off:off + T]), list(target_tokens[off:off + T])
+            off += T
+            if T == 0:
+                acc.append(0); ctx.append(int(context_lens[b])); nxt.append(-1)
+                continue
+            a = 0
+            while a + 1 < T and x[a + 1] == y[a + 1]:
+                a += 1
+            acc.append(a); ctx.append(int(context_lens[b]) + a + 1); nxt.append(int(y[a]))
+        return (np.array(acc, np.int32), np.array(ctx, np.int32), np.array(nxt, np.int32))
+    monkeypatch.setattr(O, "accept_commit", wrong)
+    assert _pins_fail(test_accept_commit_hand_cases)
+
+
+def test_lse_combine_hand_values():
+    # two splits with lse 0 and ln 3: weights 1/4 and 3/4, combined lse ln 4
+    o1 = np.array([[1.0, 0.0]])
+    o2 = np.array([[0.0, 2.0]])
+    o, lse = O.lse_combine([(o1, np.array([0.0])), (o2, np.array([np.log(3.0)]))])
+    assert abs(lse[0] - np.log(4.0)) < 1e-15
+    assert np.max(np.abs(o[0] - np.array([0.25, 1.5]))) < 1e-15
+    # an empty split (lse = -inf) has no weight
+    o, lse = O.lse_combine([(o1, np.array([0.0])), (np.full((1, 2), 7.0), np.array([-np.inf]))])
+    assert lse[0] == 0.0 and np.array_equal(o[0], o1[0])
