@@ -146,6 +146,14 @@ struct Sync {
       }
     }
   }
+  // Bounded wait that ignores the abort flag: lets copies already in flight
+  // land before the CTA exits. false = gave up.
+  __device__ __forceinline__ bool drain(uint32_t bar, uint32_t parity) const {
+    const unsigned long long t0 = global_ns();
+    while (!mbar_try_wait(bar, parity))
+      if (global_ns() - t0 > kWaitNs) return false;
+    return true;
+  }
 };
 
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
@@ -853,7 +861,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
     }
   } else if (warp >= kProducerWarp) {
     // ============================================================ producer
-    int g = 0;
+    int g = 0, armed = 0;                                   // armed: tiles staged so far
     Seg s;
     bool ok = true;
     PageWindow win;
@@ -862,8 +870,8 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
         const int r = g % kRing, sst = g % kScStages;
         const uint32_t ph = ((g / kRing) & 1) ^ 1;
         uint8_t* stage = ring + r * C::kRingStage;
-        // codes once the converters are done with tile g - 2's K and V codes,
-        // scales once the softmax is done with the scales of tile g - 3
+        // codes once the converters are done with the K and V codes of tile
+        // g - kRing, scales once the softmax is done with those of g - kScStages
         if (lane == 0)
           ok = sync.wait(smem_u32(&sh->ring_empty[0][r]), ph) &&
                sync.wait(smem_u32(&sh->ring_empty[1][r]), ph) &&
@@ -872,8 +880,20 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
         if (!ok) break;
         const int page = stage_codes<D>(p, s, it, stage, smem_u32(&sh->ring_full[r]), lane, win);
         stage_scales(p, s, page, scales + sst * 2 * kTileKeys, smem_u32(&sh->sc_full[sst]), lane);
+        ++armed;
       }
     }
+    // copies still in flight (only after an abort: on the normal path the
+    // converters consumed every staged tile) land before the CTA exits. A stage
+    // is re-armed only after its previous tile was consumed, so the last tile
+    // armed on it is its only one outstanding.
+    if (lane == 0) {
+      for (int r = 0; r < kRing && r < armed; ++r) {
+        const int last = r + ((armed - 1 - r) / kRing) * kRing;
+        sync.drain(smem_u32(&sh->ring_full[r]), (last / kRing) & 1);
+      }
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
   } else {
     // ============================================================ MMA issue
     // warps kMmaWarp / kQkOddWarp: QK(i) (i even / odd) into S[i % 2] once its
