@@ -76,7 +76,9 @@ enum {
                                          ctx + T > max_pages_per_seq * P, or
                                          sum(block_lens) > num_q_tokens */
   SPLASH_DEVICE_TIMEOUT = 3,          /* an internal wait of the tensor-core kernel gave
-                                         up after ~1 s (outputs of that call undefined) */
+                                         up (after 1 s by default, see
+                                         splash_set_wait_limit_ns); outputs of that
+                                         call undefined */
   SPLASH_DEVICE_INTERNAL = 4          /* the tensor-core kernel found its shared memory
                                          misaligned and did nothing */
 };
@@ -91,6 +93,16 @@ int splash_abi_version(void);
 /* 1 if the tensor-core attention kernel is built for this head_dim, else 0
  * (units then run on the CUDA-core kernel). */
 int splash_tensor_path_supported(int head_dim);
+
+/* Limit, in nanoseconds, of every internal pipeline wait of the tensor-core
+ * attention kernel for the launches that follow (process-wide; 0 restores the
+ * default of 1 s). When a wait runs out, the kernel stops the call's work,
+ * lets the copies and MMAs it already issued complete, frees its tensor
+ * memory, returns, and stores SPLASH_DEVICE_TIMEOUT in device_status; the
+ * outputs of that call are undefined and later calls are unaffected. Meant
+ * for tests of that path and for diagnosing a stalled GPU. Returns the
+ * previous limit. */
+unsigned long long splash_set_wait_limit_ns(unsigned long long ns);
 
 /*
  * splash_kv_append — quantise a block of new K/V rows to int8 and write them

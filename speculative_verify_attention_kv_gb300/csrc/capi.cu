@@ -1,5 +1,6 @@
 // C ABI of the library: argument validation, split planning and launches.
 // Nothing here allocates or synchronises; every launch goes to the caller's stream.
+#include <atomic>
 #include <mutex>
 
 #include "splash_common.cuh"
@@ -42,6 +43,9 @@ int device_sm_count() {
 
 bool head_dim_ok(int d) { return d == 64 || d == 128 || d == 256; }
 
+constexpr unsigned long long kDefaultWaitNs = 1000000000ull;   // 1 s
+std::atomic<unsigned long long> g_wait_limit_ns{kDefaultWaitNs};
+
 // CTAs per class: the tensor-core kernel runs one CTA per SM, the CUDA-core
 // kernel as many as fit.
 void default_ctas(int sms, int head_dim, int rows_cap, int* ncta_tc, int* ncta_simt) {
@@ -79,6 +83,10 @@ const char* splash_status_string(int status) {
 
 // 2: one interleaved K/V code pool (v_pages = k_pages + P * D)
 int splash_abi_version(void) { return 2; }
+
+unsigned long long splash_set_wait_limit_ns(unsigned long long ns) {
+  return g_wait_limit_ns.exchange(ns == 0 ? kDefaultWaitNs : ns);
+}
 
 int splash_tensor_path_supported(int head_dim) {
   return head_dim_ok(head_dim) && tc_supported(head_dim) ? 1 : 0;
@@ -250,6 +258,7 @@ static int verify_impl(
   p.num_pages = num_pages;
   p.sm_scale_log2 = sm_scale * 1.4426950408889634f;
   p.window = window;
+  p.wait_ns = g_wait_limit_ns.load();
   p.out = reinterpret_cast<__nv_bfloat16*>(out);
   p.lse = lse;
   p.ws = ws;

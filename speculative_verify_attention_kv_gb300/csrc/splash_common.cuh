@@ -121,6 +121,7 @@ struct AttnParams {
   int num_pages;
   float sm_scale_log2;            // sm_scale * log2(e)
   int window;                     // sliding window W (0: none); the planner has the same value
+  unsigned long long wait_ns;     // limit of each pipeline wait of the tensor-core kernel
   __nv_bfloat16* out;
   float* lse;
   unsigned char* ws;

@@ -16,27 +16,28 @@ namespace splash {
 constexpr int kPlanThreads = 1024;
 
 // Exclusive scan over the CTA (kPlanThreads threads); *total receives the sum.
-__device__ inline int block_exclusive_scan(int v, int* s_warp, int* total) {
+template <typename V>
+__device__ inline V block_exclusive_scan(V v, V* s_warp, V* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int incl = v;
+  V incl = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    int y = __shfl_up_sync(0xffffffffu, incl, o);
+    V y = __shfl_up_sync(0xffffffffu, incl, o);
     if (lane >= o) incl += y;
   }
   if (lane == 31) s_warp[warp] = incl;
   __syncthreads();
   if (warp == 0) {
-    int x = s_warp[lane];
+    V x = s_warp[lane];
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      int y = __shfl_up_sync(0xffffffffu, x, o);
+      V y = __shfl_up_sync(0xffffffffu, x, o);
       if (lane >= o) x += y;
     }
     s_warp[lane] = x;
   }
   __syncthreads();
-  const int res = (warp ? s_warp[warp - 1] : 0) + incl - v;
+  const V res = (warp ? s_warp[warp - 1] : V(0)) + incl - v;
   *total = s_warp[31];
   __syncthreads();
   return res;
@@ -48,6 +49,7 @@ plan_kernel(const int32_t* __restrict__ context_lens, const int32_t* __restrict_
             int tile_tc, int tile_simt, int ncta_tc, int ncta_simt, int path, int rows_bound,
             int num_q_tokens, int window, unsigned char* ws, int* device_status) {
   __shared__ int s_warp[32];
+  __shared__ long long s_warp64[32];
   const WorkspaceLayout L = make_layout(num_seqs, num_kv_heads, 0, rows_bound);
   int* q_off = reinterpret_cast<int*>(ws + L.q_off);
   int* seq_T = reinterpret_cast<int*>(ws + L.seq_T);
@@ -60,13 +62,19 @@ plan_kernel(const int32_t* __restrict__ context_lens, const int32_t* __restrict_
   const int tile[kNumClasses] = {tile_tc, tile_simt};
   const int ncta[kNumClasses] = {ncta_tc, ncta_simt};
 
-  // pass 1: per sequence — validate, classify, prefix sums of rows and tiles
-  int run_q = 0, run_t0 = 0, run_t1 = 0;
+  // pass 1: per sequence — validate, classify, prefix sums of rows and tiles.
+  // The Q / O rows of sequence b start at the sum of the caller's block_lens
+  // before it (negative lengths count as 0), whether or not b itself is valid:
+  // a rejected sequence is idle, and the others keep their rows.
+  long long run_q = 0;
+  int run_t0 = 0, run_t1 = 0;
   for (int base = 0; base < num_seqs; base += kPlanThreads) {
     const int b = base + threadIdx.x;
     int T = 0, ctx = 0, cls = -1, tiles = 0;
+    long long rows_laid_out = 0;
     if (b < num_seqs) {
       T = block_lens[b];
+      rows_laid_out = T > 0 ? T : 0;
       ctx = context_lens[b];
       const bool ok = T >= 0 && ctx >= 0 && T <= max_block_len &&
                       (long long)ctx + T <= (long long)max_pages * kPageSize;
@@ -85,10 +93,12 @@ plan_kernel(const int32_t* __restrict__ context_lens, const int32_t* __restrict_
       seq_ctx[b] = ctx;
       seq_class[b] = cls;
     }
+    long long totq;
+    const long long qo = block_exclusive_scan(rows_laid_out, s_warp64, &totq);
+    // offsets past the caller's rows only occur when the plan is dropped below
+    if (b < num_seqs) q_off[b] = (int)min(run_q + qo, (long long)num_q_tokens);
+    run_q += totq;
     int tot;
-    const int qo = block_exclusive_scan(T, s_warp, &tot);
-    if (b < num_seqs) q_off[b] = run_q + qo;
-    run_q += tot;
     const int t0 = block_exclusive_scan(cls == 0 ? tiles * num_kv_heads : 0, s_warp, &tot);
     if (b < num_seqs) stp[b] = run_t0 + t0;
     run_t0 += tot;
@@ -97,7 +107,7 @@ plan_kernel(const int32_t* __restrict__ context_lens, const int32_t* __restrict_
     run_t1 += tot;
   }
   if (threadIdx.x == 0) {
-    q_off[num_seqs] = run_q;
+    q_off[num_seqs] = (int)min(run_q, (long long)num_q_tokens);
     stp[num_seqs] = run_t0;
     stp[(num_seqs + 1) + num_seqs] = run_t1;
   }

@@ -63,7 +63,9 @@ static_assert(kThreads == 512, "warp roles");
 static_assert(kStages == 2, "one QK-issuing warp per S/P buffer");
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.0f;          // lazy rescale threshold (factor 256)
-constexpr unsigned long long kWaitNs = 1000000000ull;
+// limit of the drain waits (copies and MMAs already issued land before the
+// CTA frees its TMEM and exits); the pipeline waits use AttnParams::wait_ns
+constexpr unsigned long long kDrainNs = 1000000000ull;
 
 template <int D>
 struct Cfg {
@@ -132,6 +134,7 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
 struct Sync {
   volatile int* abort_flag;
   int* status;
+  unsigned long long limit_ns;
   // Bounded wait for the phase of `parity` to complete. false = gave up.
   __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity) const {
     if (mbar_try_wait(bar, parity)) return true;
@@ -139,7 +142,7 @@ struct Sync {
     while (true) {
       if (mbar_try_wait(bar, parity)) return true;
       if (*abort_flag) return false;
-      if (global_ns() - t0 > kWaitNs) {
+      if (global_ns() - t0 > limit_ns) {
         *abort_flag = 1;
         report(status, SPLASH_DEVICE_TIMEOUT);
         return false;
@@ -151,7 +154,7 @@ struct Sync {
   __device__ __forceinline__ bool drain(uint32_t bar, uint32_t parity) const {
     const unsigned long long t0 = global_ns();
     while (!mbar_try_wait(bar, parity))
-      if (global_ns() - t0 > kWaitNs) return false;
+      if (global_ns() - t0 > kDrainNs) return false;
     return true;
   }
 };
@@ -555,7 +558,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
   __syncthreads();
   fence_after();
   const uint32_t tmem = sh->tmem_base;
-  const Sync sync{&sh->abort_flag, p.device_status};
+  const Sync sync{&sh->abort_flag, p.device_status, p.wait_ns};
 
   const int window = kSwa ? p.window : 0;
   SegIter iter{stp, seq_T, seq_ctx, B, G, Hkv, window, tile_begin(blockIdx.x, total, ncta),
@@ -952,9 +955,11 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
         }
         ++nsegs;
       }
-      // every MMA this thread issued is complete before TMEM is released
+      // every MMA this thread issued is complete before TMEM is released and
+      // the shared-memory operands go away; the drain wait ignores the abort
+      // flag (after an abort the MMAs already issued still run to completion)
       mma_commit(smem_u32(&sh->drain[role]));
-      sync.wait(smem_u32(&sh->drain[role]), 0);
+      sync.drain(smem_u32(&sh->drain[role]), 0);
     }
     __syncwarp();
   }

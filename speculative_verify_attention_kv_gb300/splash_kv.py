@@ -18,6 +18,7 @@ _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libsplashk
 PAGE_SIZE = 16
 DEVICE_BAD_PAGE = 1
 DEVICE_BAD_LENGTH = 2
+DEVICE_TIMEOUT = 3
 PATH_AUTO, PATH_SIMT, PATH_TENSOR = 0, 1, 2
 
 
@@ -39,6 +40,8 @@ def _load() -> ctypes.CDLL:
     lib.splash_abi_version.restype = I
     lib.splash_tensor_path_supported.restype = I
     lib.splash_tensor_path_supported.argtypes = [I]
+    lib.splash_set_wait_limit_ns.restype = ctypes.c_ulonglong
+    lib.splash_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
     lib.splash_kv_append.restype = I
     lib.splash_kv_append.argtypes = [P, P, I, P, P, P, P, P, I, P, P, I, I, I, I, I, P, P]
     lib.splash_kv_append_bf16.restype = I
@@ -65,6 +68,7 @@ def _load() -> ctypes.CDLL:
 
 LIB = _load()
 EXPORTED = ("splash_status_string", "splash_abi_version", "splash_tensor_path_supported",
+            "splash_set_wait_limit_ns",
             "splash_kv_append", "splash_kv_append_bf16", "splash_accept_commit",
             "splash_verify_attention_swa",
             "splash_verify_attention_workspace_size", "splash_verify_attention",
@@ -74,6 +78,12 @@ EXPORTED = ("splash_status_string", "splash_abi_version", "splash_tensor_path_su
 
 def tensor_path_available(head_dim: int) -> bool:
     return bool(LIB.splash_tensor_path_supported(int(head_dim)))
+
+
+def splash_set_wait_limit_ns(ns: int) -> int:
+    """Limit of each internal wait of the tensor-core kernel for later launches
+    (0 = the default of 1 s); returns the previous limit."""
+    return int(LIB.splash_set_wait_limit_ns(int(ns)))
 
 
 def status_string(status: int) -> str:

@@ -51,6 +51,16 @@ def test_status_strings(sk):
     assert sk.LIB.splash_abi_version() == 2
 
 
+def test_wait_limit_setter_round_trips(sk):
+    prev = sk.splash_set_wait_limit_ns(12345)
+    try:
+        assert prev == 10 ** 9
+        assert sk.splash_set_wait_limit_ns(0) == 12345      # 0 restores the default
+        assert sk.splash_set_wait_limit_ns(0) == 10 ** 9
+    finally:
+        sk.splash_set_wait_limit_ns(0)
+
+
 FAKE = ctypes.c_void_p(256)  # never dereferenced: validation fails first
 FAKE_V = ctypes.c_void_p(256 + 16 * 128)   # V half of the code pool at D = 128: K + P*D
 

@@ -350,6 +350,53 @@ def test_bad_length_sets_device_status():
     assert int(r.status.item()) == sk.DEVICE_BAD_LENGTH
 
 
+def test_bad_sequence_leaves_the_others_correct():
+    # the middle sequence's length exceeds its page-table capacity: it is
+    # skipped, and the sequences after it keep their own Q / O rows
+    W = wl.custom(24, 4, 256, [300, 500, 700], [4, 8, 16], seed=52)
+    r = Run(W)
+    r.append_block()
+    o_ref, l_ref = oracle_attention(W, oracle_pool(W))
+    ctx = r.ctx.clone()
+    ctx[1] = W.max_pages_per_seq * 16
+    r.ctx = ctx
+    rows = seq_rows(W, [0, 2])
+    for path in PATHS:
+        if not _path_ok(path):
+            continue
+        r.status.zero_()
+        o, l = r.attend(path=path)
+        torch.cuda.synchronize()
+        assert int(r.status.item()) == sk.DEVICE_BAD_LENGTH
+        assert_parity(o, l, o_ref, l_ref, rows=rows, what=f"path {path}")
+
+
+def test_wait_timeout_is_reported_and_the_next_call_is_correct():
+    # A wait limit of 1 ns makes the tensor-core kernel's first pipeline wait
+    # run out: it must stop, let the copies and MMAs it issued complete, free
+    # its tensor memory and report SPLASH_DEVICE_TIMEOUT; the following call
+    # with the default limit must be unaffected.
+    if not _path_ok(sk.PATH_TENSOR):
+        pytest.skip("tensor-core kernel not built")
+    W, r = _small_run(seed=53)
+    o_ref, l_ref = oracle_attention(W, oracle_pool(W))
+    for _ in range(2):
+        prev = sk.splash_set_wait_limit_ns(1)
+        try:
+            r.status.zero_()
+            r.attend(path=sk.PATH_TENSOR)
+            torch.cuda.synchronize()
+            st = int(r.status.item())
+        finally:
+            sk.splash_set_wait_limit_ns(prev)
+        assert st == sk.DEVICE_TIMEOUT
+        r.status.zero_()
+        o, l = r.attend(path=sk.PATH_TENSOR)
+        torch.cuda.synchronize()
+        assert int(r.status.item()) == 0
+        assert_parity(o, l, o_ref, l_ref, what="after a timeout")
+
+
 def test_workspace_too_small():
     W, r = _small_run(ctx=(300,), T=(4,))
     r.ws = r.ws[:1024]
@@ -383,7 +430,11 @@ def test_sliding_window_matches_oracle(path, window):
     for ctas in (0, 1, 5):
         o, l = r.attend(path=path, ctas=ctas, window=window)
         torch.cuda.synchronize()
-        assert_parity_scaled(o, l, o_ref, l_ref, what=f"window {window} path {path} ctas {ctas}")
+        what = f"window {window} path {path} ctas {ctas}"
+        if window >= 64:
+            assert_parity(o, l, o_ref, l_ref, what=what)
+        else:   # rows that see fewer than 64 keys: bound scaled with |O|
+            assert_parity_scaled(o, l, o_ref, l_ref, what=what)
     assert int(r.status.item()) == 0
 
 
