@@ -3,6 +3,8 @@
 #include <atomic>
 #include <mutex>
 
+#include <cuda.h>
+
 #include "splash_common.cuh"
 
 namespace splash {
@@ -22,6 +24,10 @@ cudaError_t launch_verify_simt(const AttnParams&, int, int, cudaStream_t);
 size_t simt_smem_bytes(int, int);
 cudaError_t launch_verify_tc(const AttnParams&, int, int, cudaStream_t);
 bool tc_supported(int head_dim);
+bool tt_supported(int head_dim, int rows_cap);
+int tt_tile_keys();
+bool tt_encode_map(CUtensorMap* map, const int8_t* k_pages, int num_pages, int num_kv_heads);
+cudaError_t launch_verify_tt(const AttnParams&, const CUtensorMap&, int, cudaStream_t);
 constexpr int kSimtTile = 64;
 constexpr int kTcTile = 64;
 
@@ -199,7 +205,7 @@ static int verify_impl(
   int st = check_attn_shape(num_q_tokens, num_seqs, num_q_heads, num_kv_heads, head_dim,
                             page_size, max_block_len, max_pages_per_seq);
   if (st != SPLASH_OK) return st;
-  if (path < 0 || path > 2 || ctas_per_class < 0 || num_pages < 0 || window < 0)
+  if (path < 0 || path > 3 || ctas_per_class < 0 || num_pages < 0 || window < 0)
     return SPLASH_ERR_INVALID_ARGUMENT;
   if (num_q_tokens == 0 || num_seqs == 0) return SPLASH_OK;
   if (k_pages && v_pages && v_pages != k_pages + (size_t)page_size * head_dim)
@@ -214,6 +220,16 @@ static int verify_impl(
   if (!(sm_scale > 0.f) || sm_scale == INFINITY) return SPLASH_ERR_INVALID_ARGUMENT;
   const bool tc_ok = tc_supported(head_dim);
   if (path == 2 && !tc_ok) return SPLASH_ERR_UNSUPPORTED;
+  if (path == 3 && !tt_supported(head_dim, rows_cap)) return SPLASH_ERR_UNSUPPORTED;
+  // the transposed tensor-core kernel takes head_dim 256 with at most 96 rows
+  // per unit (path 3); it reads the codes through a tensor map
+  CUtensorMap tmap;
+  bool use_tt = false;
+  if (path == 3 && tt_supported(head_dim, rows_cap)) {
+    use_tt = tt_encode_map(&tmap, k_pages, num_pages, num_kv_heads);
+    if (!use_tt && path == 3) return SPLASH_ERR_INVALID_ARGUMENT;
+  }
+  if (path == 3) path = 2;
   if (!tc_ok) path = 1;
   // rows the CUDA-core kernel may see: all (path 1), none (path 2), fewer than
   // kTensorMinRows (automatic)
@@ -238,7 +254,8 @@ static int verify_impl(
   // for every unit with >= 16 rows).
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = launch_plan(context_lens, block_lens, num_seqs, num_kv_heads, G,
-                              max_pages_per_seq, max_block_len, kTcTile, kSimtTile, nt, ns, path,
+                              max_pages_per_seq, max_block_len, use_tt ? tt_tile_keys() : kTcTile,
+                              kSimtTile, nt, ns, path,
                               (int)rb, num_q_tokens, window, ws, device_status, s);
   if (e != cudaSuccess) return SPLASH_ERR_CUDA;
 
@@ -266,7 +283,7 @@ static int verify_impl(
   if (attn_begin && cudaEventRecord(reinterpret_cast<cudaEvent_t>(attn_begin), s) != cudaSuccess)
     return SPLASH_ERR_CUDA;
   if (path != 1 && tc_ok) {
-    e = launch_verify_tc(p, rows_cap, nt, s);
+    e = use_tt ? launch_verify_tt(p, tmap, nt, s) : launch_verify_tc(p, rows_cap, nt, s);
     if (e != cudaSuccess) return SPLASH_ERR_CUDA;
   }
   if (path != 2 && rows_simt > 0) {

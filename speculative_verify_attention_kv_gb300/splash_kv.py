@@ -19,7 +19,11 @@ PAGE_SIZE = 16
 DEVICE_BAD_PAGE = 1
 DEVICE_BAD_LENGTH = 2
 DEVICE_TIMEOUT = 3
-PATH_AUTO, PATH_SIMT, PATH_TENSOR = 0, 1, 2
+PATH_AUTO, PATH_SIMT, PATH_TENSOR, PATH_TENSOR_T = 0, 1, 2, 3
+# PATH_TENSOR: tensor-core kernel with the query rows on the MMA's M side (any
+# head_dim of 128 / 256, up to 128 rows); PATH_TENSOR_T: the transposed kernel
+# (keys on M, rows on N; head_dim 256, up to 96 rows per unit), which automatic
+# mode picks whenever it applies
 
 
 class SplashError(RuntimeError):

@@ -64,11 +64,15 @@ def _tc_probe():
     return True
 
 
-PATHS = [sk.PATH_AUTO, sk.PATH_SIMT, sk.PATH_TENSOR]
+PATHS = [sk.PATH_AUTO, sk.PATH_SIMT, sk.PATH_TENSOR, sk.PATH_TENSOR_T]
 
 
-def _path_ok(path, head_dim=256):
-    return path != sk.PATH_TENSOR or sk.tensor_path_available(head_dim)
+def _path_ok(path, head_dim=256, rows=96):
+    if path == sk.PATH_TENSOR:
+        return sk.tensor_path_available(head_dim)
+    if path == sk.PATH_TENSOR_T:
+        return head_dim == 256 and rows <= 96
+    return True
 
 
 # ---------------------------------------------------------------------------
@@ -187,8 +191,8 @@ SMALL = [
 @pytest.mark.parametrize("path", PATHS)
 def test_attention_small_cases(case, path):
     c = SMALL[case]
-    if not _path_ok(path, c["D"]):
-        pytest.skip("tensor-core kernel not built for this head_dim")
+    if not _path_ok(path, c["D"], max(c["T"]) * c["hq"] // c["hkv"]):
+        pytest.skip("kernel not built for this head_dim / row count")
     W = wl.custom(c["hq"], c["hkv"], c["D"], c["ctx"], c["T"], seed=20 + case,
                   shared_prefix_len=c.get("prefix", 0))
     r = Run(W)
@@ -371,12 +375,13 @@ def test_bad_sequence_leaves_the_others_correct():
         assert_parity(o, l, o_ref, l_ref, rows=rows, what=f"path {path}")
 
 
-def test_wait_timeout_is_reported_and_the_next_call_is_correct():
+@pytest.mark.parametrize("path", [sk.PATH_TENSOR, sk.PATH_TENSOR_T])
+def test_wait_timeout_is_reported_and_the_next_call_is_correct(path):
     # A wait limit of 1 ns makes the tensor-core kernel's first pipeline wait
     # run out: it must stop, let the copies and MMAs it issued complete, free
     # its tensor memory and report SPLASH_DEVICE_TIMEOUT; the following call
     # with the default limit must be unaffected.
-    if not _path_ok(sk.PATH_TENSOR):
+    if not _path_ok(path):
         pytest.skip("tensor-core kernel not built")
     W, r = _small_run(seed=53)
     o_ref, l_ref = oracle_attention(W, oracle_pool(W))
@@ -384,14 +389,14 @@ def test_wait_timeout_is_reported_and_the_next_call_is_correct():
         prev = sk.splash_set_wait_limit_ns(1)
         try:
             r.status.zero_()
-            r.attend(path=sk.PATH_TENSOR)
+            r.attend(path=path)
             torch.cuda.synchronize()
             st = int(r.status.item())
         finally:
             sk.splash_set_wait_limit_ns(prev)
         assert st == sk.DEVICE_TIMEOUT
         r.status.zero_()
-        o, l = r.attend(path=sk.PATH_TENSOR)
+        o, l = r.attend(path=path)
         torch.cuda.synchronize()
         assert int(r.status.item()) == 0
         assert_parity(o, l, o_ref, l_ref, what="after a timeout")
