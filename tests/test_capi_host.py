@@ -98,7 +98,8 @@ def _attn(sk, **kw):
 @pytest.mark.parametrize("kw,code", [
     (dict(hq=7), -1), (dict(hkv=0), -1), (dict(D=100), -2), (dict(P=32), -2),
     (dict(maxT=40), -2),              # T*G = 160 > 128 rows
-    (dict(maxT=-1), -1), (dict(n=-3), -1), (dict(maxp=0), -1), (dict(path=3), -1),
+    (dict(maxT=-1), -1), (dict(n=-3), -1), (dict(maxp=0), -1), (dict(path=4), -1),
+    (dict(path=3), -2),               # the transposed kernel takes head_dim 256 only
     (dict(ctas=-1), -1), (dict(q=None), -1), (dict(ws=None), -1), (dict(lse=None), -1),
     (dict(ws=ctypes.c_void_p(256 + 16)), -1),   # workspace not 256-byte aligned
     (dict(n=0), 0), (dict(B=0), 0),
@@ -139,7 +140,7 @@ def test_sliding_window_argument_errors(sk):
     tail = [FAKE, FAKE, FAKE, 1 << 30, None, None, 0, 0]
     f = sk.LIB.splash_verify_attention_swa
     assert f(*args, -1, *tail) == -1                      # negative window
-    assert f(*args, 5, FAKE, FAKE, FAKE, 1 << 30, None, None, 3, 0) == -1   # bad path
+    assert f(*args, 5, FAKE, FAKE, FAKE, 1 << 30, None, None, 4, 0) == -1   # bad path
     args_bad_pool = list(args)
     args_bad_pool[3] = FAKE                                # V codes not at K + P*D
     assert f(*args_bad_pool, 5, *tail) == -1
