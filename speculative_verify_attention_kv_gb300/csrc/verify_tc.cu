@@ -119,6 +119,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// One arrival per warp: every lane's prior writes (and tcgen05 / proxy fences)
+// are ordered before lane 0's release by the warp barrier.
+__device__ __forceinline__ void warp_arrive(uint32_t bar, int lane) {
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bar);
+}
+
 __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -526,24 +533,24 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
   if (tid == 0) {
     for (int s = 0; s < kRing; ++s) {
       mbar_init(smem_u32(&sh->ring_full[s]), 1);
-      for (int kv = 0; kv < 2; ++kv) mbar_init(smem_u32(&sh->ring_empty[kv][s]), kLoadThreads);
+      for (int kv = 0; kv < 2; ++kv) mbar_init(smem_u32(&sh->ring_empty[kv][s]), kLoadWarps);
     }
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(smem_u32(&sh->k_full[s]), kLoadThreads);
+      mbar_init(smem_u32(&sh->k_full[s]), kLoadWarps);
       mbar_init(smem_u32(&sh->k_free[s]), 1);
       mbar_init(smem_u32(&sh->s_full[s]), 1);
-      mbar_init(smem_u32(&sh->p_full[s]), 32 * kSoftmaxWarps);
+      mbar_init(smem_u32(&sh->p_full[s]), kSoftmaxWarps);
       mbar_init(smem_u32(&sh->p_free[s]), 1);
     }
     for (int s = 0; s < kScStages; ++s) {
       mbar_init(smem_u32(&sh->sc_full[s]), 32);     // one cp.async arrival per producer lane
-      mbar_init(smem_u32(&sh->sc_free[s]), 32 * kSoftmaxWarps);
+      mbar_init(smem_u32(&sh->sc_free[s]), kSoftmaxWarps);
     }
     for (int s = 0; s < kVStages; ++s) {
       mbar_init(smem_u32(&sh->v_free[s]), 1);
-      mbar_init(smem_u32(&sh->v_full[s]), kLoadThreads);
+      mbar_init(smem_u32(&sh->v_full[s]), kLoadWarps);
     }
-    mbar_init(smem_u32(&sh->q_full), 32 * kSoftmaxWarps);
+    mbar_init(smem_u32(&sh->q_full), kSoftmaxWarps);
     mbar_init(smem_u32(&sh->q_ack), 2);
     for (int i = 0; i < 3; ++i) mbar_init(smem_u32(&sh->drain[i]), 1);
     sh->abort_flag = 0;
@@ -566,10 +573,11 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
 
   if (warp < kSoftmaxWarps) {
     // ===================================================== softmax + epilogue
-    const int lb = 32 * (warp % 4) + 16 * (warp / 4);     // first TMEM lane (row) of the warp
+    const int lb = 32 * (warp % 4) + 16 * (warp / 4);     // first TMEM lane of the warp
     const uint32_t lane_base = (uint32_t)lb << 16;
     const int quad = lane & 3;                            // column pair within 8 columns
-    const int rr[2] = {lb + (lane >> 2), lb + 8 + (lane >> 2)};
+    // TMEM lanes of this thread's two rows
+    const int ln[2] = {lb + (lane >> 2), lb + 8 + (lane >> 2)};
     int g = 0, nsegs = 0;
     Seg s;
     bool ok = true;
@@ -577,22 +585,31 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
       // Q' of this segment overwrites the previous one: both QK issuers must
       // have seen the previous q_full phase (so neither lags it by two phases)
       if (nsegs > 0) {
-        ok = sync.wait(smem_u32(&sh->q_ack), (nsegs - 1) & 1);
+        ok = __all_sync(0xffffffffu, sync.wait(smem_u32(&sh->q_ack), (nsegs - 1) & 1));
         if (!ok) break;
       }
       ++nsegs;
-      const bool warp_live = lb < s.R;
+      // The unit's rows are spread evenly over the four TMEM lane quarters
+      // (each served by the softmax warps of one SM sub-partition): row
+      // q * rpq + i sits in lane 32q + i, i < rpq = ceil(R / 4). Lanes past
+      // rpq in a quarter hold no row.
+      const int rpq = (s.R + 3) >> 2;
+      int rr[2];                                          // row of each of this thread's lanes, -1: none
       bool live[2];
       int lim[2], lo[2];
       size_t qrow_off[2];
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
-        live[k] = rr[k] < s.R;
-        const int tt = rr[k] / G, gg = rr[k] % G;
+        const int i = ln[k] & 31, r = (ln[k] >> 5) * rpq + i;
+        live[k] = i < rpq && r < s.R;
+        rr[k] = live[k] ? r : -1;
+        const int tt = live[k] ? r / G : 0, gg = live[k] ? r - tt * G : 0;
         lim[k] = s.ctx + tt;                              // last visible key of the row
         lo[k] = kSwa ? lim[k] - window + 1 : 0;           // first visible key (with a window)
         qrow_off[k] = (size_t)(q_off[s.b] + tt) * p.num_q_heads + s.h * G + gg;
       }
+      const bool warp_live = __any_sync(0xffffffffu, live[0]);
+      const bool k1_live = __any_sync(0xffffffffu, live[1]);   // second row set of the warp
       float rowfac[2] = {0.f, 0.f};
       // Q rows -> TMEM as fp16 after an exact per-row power-of-two rescale.
       // Thread covers d = 8i + 2*quad + {0,1} (i < D/8) of both rows; all of
@@ -647,13 +664,14 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
         tmem_wait_st();
       }
       fence_before();
-      mbar_arrive(smem_u32(&sh->q_full));
+      warp_arrive(smem_u32(&sh->q_full), lane);
 
       float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};   // l: this thread's columns
       for (int it = s.i0; it < s.i1 && ok; ++it, ++g) {
         const int st = g % kStages, sst = g % kScStages;
         ok = sync.wait(smem_u32(&sh->sc_full[sst]), (g / kScStages) & 1) &&
              sync.wait(smem_u32(&sh->s_full[st]), (g / kStages) & 1);
+        ok = __all_sync(0xffffffffu, ok);       // a timeout seen by some lanes stops the warp
         if (!ok) break;
         fence_after();
         uint32_t pw[16];                                   // P: 32 packed columns
@@ -680,8 +698,10 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
           for (int i = 0; i < 8; ++i) {
 #pragma unroll
             for (int k = 0; k < 2; ++k)
-              x[k][i] = __fmul2_rn(make_float2(__uint_as_float(sv[4 * i + 2 * k]),
-                                               __uint_as_float(sv[4 * i + 2 * k + 1])), ks2[i]);
+              x[k][i] = (k == 0 || k1_live)
+                            ? __fmul2_rn(make_float2(__uint_as_float(sv[4 * i + 2 * k]),
+                                                     __uint_as_float(sv[4 * i + 2 * k + 1])), ks2[i])
+                            : make_float2(-INFINITY, -INFINITY);
           }
           // tile keys jj with nlo <= jj < nvis are visible to the row
           int nvis[2], nlo[2];
@@ -690,7 +710,9 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
           for (int k = 0; k < 2; ++k) {
             nvis[k] = live[k] ? min(kTileKeys, lim[k] - k0 + 1) : 0;
             nlo[k] = kSwa ? max(lo[k] - k0, -1) : -1;         // compile-time -1 without a window
-            full = full && nvis[k] == kTileKeys && (!kSwa || nlo[k] <= 0);
+            // rows that hold no query row need no mask (their P only reaches
+            // output rows that are never read)
+            full = full && (!live[k] || (nvis[k] == kTileKeys && (!kSwa || nlo[k] <= 0)));
           }
           if (!full) {
 #pragma unroll
@@ -702,9 +724,10 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
                 if (j + 1 >= nvis[k] || j + 1 < nlo[k]) x[k][i].y = -INFINITY;
               }
           }
-          float base[2];
+          float base[2] = {0.f, 0.f};
 #pragma unroll
           for (int k = 0; k < 2; ++k) {
+            if (k == 1 && !k1_live) break;                // no row in the warp's second set
             float mt = -INFINITY;
 #pragma unroll
             for (int i = 0; i < 8; ++i) mt = fmax3(mt, x[k][i].x, x[k][i].y);
@@ -730,6 +753,11 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
           }
 #pragma unroll
           for (int k = 0; k < 2; ++k) {
+            if (k == 1 && !k1_live) {
+#pragma unroll
+              for (int i = 0; i < 8; ++i) pw[2 * i + 1] = 0u;
+              break;
+            }
             const float2 rf2 = make_float2(rowfac[k], rowfac[k]);
             const float2 nb2 = make_float2(-base[k], -base[k]);
             float2 acc = make_float2(0.f, 0.f);
@@ -756,7 +784,8 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
         // so a parity wait cannot be satisfied by an older phase.
         if (it > s.i0 && warp_live &&
             __any_sync(0xffffffffu, alpha[0] != 1.f || alpha[1] != 1.f)) {
-          ok = sync.wait(smem_u32(&sh->p_free[(g - 1) % kStages]), ((g - 1) / kStages) & 1);
+          ok = __all_sync(0xffffffffu,
+                          sync.wait(smem_u32(&sh->p_free[(g - 1) % kStages]), ((g - 1) / kStages) & 1));
           if (!ok) break;
           fence_after();
 #pragma unroll 1
@@ -775,17 +804,18 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
             tmem_st16x256_x8(tmem + lane_base + C::kOCol + c0, v);
           }
         }
-        mbar_arrive(smem_u32(&sh->sc_free[sst]));          // scales of this tile are read
+        warp_arrive(smem_u32(&sh->sc_free[sst]), lane);    // scales of this tile are read
         if (warp_live) {
           tmem_st16x128_x8(tmem + lane_base + C::kSCol + st * kTileKeys, pw);
           tmem_wait_st();
         }
         fence_before();
-        mbar_arrive(smem_u32(&sh->p_full[st]));
+        warp_arrive(smem_u32(&sh->p_full[st]), lane);
       }
       if (!ok) break;
       // epilogue: last PV of the segment complete -> normalise, write out
-      ok = sync.wait(smem_u32(&sh->p_free[(g - 1) % kStages]), ((g - 1) / kStages) & 1);
+      ok = __all_sync(0xffffffffu,
+                      sync.wait(smem_u32(&sh->p_free[(g - 1) % kStages]), ((g - 1) / kStages) & 1));
       if (!ok) break;
       fence_after();
       if (warp_live) {
@@ -848,18 +878,25 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
         // K codes -> fp16 K tile; the QK of the tile may start at once
         ok = sync.wait(smem_u32(&sh->ring_full[r]), ph) &&
              sync.wait(smem_u32(&sh->k_free[st]), ((g / kStages) & 1) ^ 1);
+        ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         convert_codes<D>(stage, kbuf + st * C::kTileBytes, lt);
-        mbar_arrive(smem_u32(&sh->ring_empty[0][r]));
         fence_async_smem();
-        mbar_arrive(smem_u32(&sh->k_full[st]));
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(smem_u32(&sh->ring_empty[0][r]));
+          mbar_arrive(smem_u32(&sh->k_full[st]));
+        }
         // V codes -> fp16 V tile
-        ok = sync.wait(smem_u32(&sh->v_free[vst]), ((g / kVStages) & 1) ^ 1);
+        ok = __all_sync(0xffffffffu, sync.wait(smem_u32(&sh->v_free[vst]), ((g / kVStages) & 1) ^ 1));
         if (!ok) break;
         convert_codes<D>(stage + kPageSize * D, vbuf + vst * C::kTileBytes, lt);
-        mbar_arrive(smem_u32(&sh->ring_empty[1][r]));
         fence_async_smem();
-        mbar_arrive(smem_u32(&sh->v_full[vst]));
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(smem_u32(&sh->ring_empty[1][r]));
+          mbar_arrive(smem_u32(&sh->v_full[vst]));
+        }
       }
     }
   } else if (warp >= kProducerWarp) {

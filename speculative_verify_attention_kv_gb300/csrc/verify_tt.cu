@@ -35,14 +35,15 @@
 //   warps 0-7   softmax + epilogue: warp w reads TMEM lane quarter w%4 (keys
 //               32(w%4)..+31 of the tile), columns (rows) 48(w/4)..+47
 //   warps 8-11  K converters: warp 8+q issues the tensor-map loads of its two
-//               pages of each tile (two tiles ahead, swizzled staging), then
-//               turns its 32 keys' int8 K codes into the fp16 A operand in
-//               TMEM lanes 32q..+31
-//   warps 12-13 V converters: int8 V codes -> fp16 V^T, 32 keys at a time
+//               pages of each tile and their K / V scales (cp.async), two
+//               tiles ahead (swizzled staging), then turns its 32 keys' int8
+//               K codes into the fp16 A operand in TMEM lanes 32q..+31
+//   warps 12,13,15  V converters: int8 V codes -> fp16 V^T, 16 keys at a
+//               time into a ring of 4 buffers (conversion runs up to half a
+//               tile ahead of PV); warp 12 also issues the V-code tensor-map
+//               loads (4 pages = 64 keys per stage)
 //   warp  14    lane 0 issues every MMA: QK^T (16 per tile) and PV (16 per
-//               tile, 4 per 32 keys), whichever is ready first
-//   warp  15    producer: V-code tensor-map loads (4 pages = 64 keys per
-//               stage) and the K / V scales (cp.async)
+//               tile, 2 per 16 keys), whichever is ready first
 // TMEM (512 columns): K^ 128 | S^T x2 (96 each) | O^T d-halves x2 (96 each).
 // Every cross-warp handshake is an mbarrier with a bounded wait.
 #include <cuda.h>
@@ -57,18 +58,19 @@ using namespace dev;
 constexpr int D = 256;
 constexpr int kTileKeys = 128;
 constexpr int kNMax = 96;                  // query rows per unit this kernel takes
-constexpr int kSubKeys = 64;               // keys per V stage and per scale slot
-constexpr int kQtrKeys = 32;               // keys per V^T buffer (one PV step)
+constexpr int kSubKeys = 64;               // keys per V stage
+constexpr int kVtKeys = 16;                // keys per V^T buffer (one PV step)
+constexpr int kVtBufs = 4;
 constexpr int kSoftmaxWarps = 8;
 constexpr int kSoftmaxThreads = 32 * kSoftmaxWarps;
 constexpr int kKConvWarp0 = 8;
-constexpr int kVConvWarp0 = 12;
-constexpr int kVConvThreads = 64;
+constexpr int kVConvWarp0 = 12;            // warps 12, 13 and 15
+constexpr int kVConvThreads = 96;
 constexpr int kMmaWarp = 14;
 constexpr int kThreads = 512;
 constexpr int kKDepth = 2;                 // tiles of K staging per K converter
 constexpr int kVRing = 2;                  // V stages (64 keys each)
-constexpr int kScSlots = 4;                // scale slots (64 keys each)
+constexpr int kScSlots = 4;                // scale slots (one tile each)
 constexpr float kPTop = 7.0f;              // a slow path puts the tile's largest P at 2^7
 constexpr float kPLimit = 15.0f;           // fast path while P <= 2^15 (fp16 max ~2^16)
 constexpr float kWLimit = 100.0f;          // and the weights w stay <= 2^100 (fp32 sums)
@@ -89,18 +91,18 @@ constexpr int kPageHalf = 16 * 128;                    // one half of 16 rows: 2
 constexpr int kPageBytes = 2 * kPageHalf;              // 16 rows x 256 B: 4 KB
 constexpr int kKStage = 2 * kPageBytes;                // a K converter's 2 pages: 8 KB
 constexpr int kVStage = 4 * kPageBytes;                // 4 pages: 16 KB
-constexpr int kVtBytes = D * kQtrKeys * 2;             // V^T [d-atom 4][key 32][128 B]: 16 KB
-constexpr int kVtAtom = kQtrKeys * 128;                // 4 KB
+constexpr int kVtBytes = D * kVtKeys * 2;              // V^T [d-atom 4][key 16][128 B]: 8 KB
+constexpr int kVtAtom = kVtKeys * 128;                 // 2 KB
 constexpr int kPHalfBytes = 2 * kSubKeys * 128;        // P^T [row-atom 2][key 64][128 B]: 16 KB
 constexpr int kPAtom = kSubKeys * 128;                 // 8 KB
 constexpr int kQAtom = kNMax * 128;                    // Q'^T [d-atom 4][row 96][128 B]: 12 KB
 constexpr int kOffKst = 0;
 constexpr int kOffVst = kOffKst + 4 * kKDepth * kKStage;
 constexpr int kOffVt = kOffVst + kVRing * kVStage;
-constexpr int kOffP = kOffVt + 2 * kVtBytes;
+constexpr int kOffP = kOffVt + kVtBufs * kVtBytes;
 constexpr int kOffQ = kOffP + 2 * kPHalfBytes;
-constexpr int kOffSc = kOffQ + 4 * kQAtom;             // [slot][K 64 | V 64] fp32
-constexpr int kOffRed = kOffSc + kScSlots * 2 * kSubKeys * 4;
+constexpr int kOffSc = kOffQ + 4 * kQAtom;             // [slot][K 128 | V 128] fp32
+constexpr int kOffRed = kOffSc + kScSlots * 2 * kTileKeys * 4;
 constexpr int kRedBytes = (4 * 128 + 3 * 128 + 64) * 4;
 constexpr int kOffBars = kOffRed + kRedBytes;
 constexpr int kBarBytes = 512;
@@ -124,22 +126,22 @@ static_assert(sizeof(Red) <= kRedBytes, "scratch");
 
 struct Bars {
   uint64_t kst_full[4][kKDepth];  // K converter q's copies of a tile landed (tx)
-  uint64_t kt_full;               // K^ of the tile in TMEM (128 arrivals)
+  uint64_t kt_full;               // K^ of the tile in TMEM (one arrival per warp)
   uint64_t kt_free;               // QK^T done reading K^ (MMA commit)
   uint64_t vst_full[kVRing];      // V stage landed (tx)
-  uint64_t vst_empty[kVRing];     // V converters done with a stage (64)
-  uint64_t sc_full[kScSlots];     // scales landed (32 cp.async arrivals)
-  uint64_t sc_free[kScSlots];     // softmax done with the scales (128)
+  uint64_t vst_empty[kVRing];     // V converters done with a stage (3 warps)
+  uint64_t sc_full[kScSlots];     // scales of a tile landed (128 cp.async arrivals)
+  uint64_t sc_free[kScSlots];     // softmax done with the scales (8 warps)
   uint64_t s_full[2];             // QK^T done (commit)
-  uint64_t s_free[2];             // softmax done reading S^T (256)
-  uint64_t p_full[2];             // P^T half written (128)
+  uint64_t s_free[2];             // softmax done reading S^T (8 warps)
+  uint64_t p_full[2];             // P^T half written (4 warps)
   uint64_t p_free[2];             // PV of that half done (commit)
-  uint64_t vt_full[2];            // V^T buffer written (64)
-  uint64_t vt_free[2];            // PV of that buffer done (commit)
+  uint64_t vt_full[kVtBufs];      // V^T buffer written (3 warps)
+  uint64_t vt_free[kVtBufs];      // PV of that buffer done (commit)
   uint64_t o_done[2];             // all PVs of a tile done (commit), by tile parity
-  uint64_t o_free;                // epilogue done reading O^T (256)
-  uint64_t q_full;                // Q'^T of the segment in smem (256)
-  uint64_t smx;                   // barrier of the softmax warps (256)
+  uint64_t o_free;                // epilogue done reading O^T (8 warps)
+  uint64_t q_full;                // Q'^T of the segment in smem (8 warps)
+  uint64_t smx;                   // barrier of the softmax warps (8 warps)
   uint64_t drain;                 // the MMA issuer's MMAs complete
   uint32_t tmem_base;
   int abort_flag;
@@ -289,28 +291,30 @@ verify_tt_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmap) {
   if (tid == 0) {
     for (int q = 0; q < 4; ++q)
       for (int d = 0; d < kKDepth; ++d) mbar_init(smem_u32(&sh->kst_full[q][d]), 1);
-    mbar_init(smem_u32(&sh->kt_full), 128);
+    mbar_init(smem_u32(&sh->kt_full), 4);
     mbar_init(smem_u32(&sh->kt_free), 1);
     for (int i = 0; i < kVRing; ++i) {
       mbar_init(smem_u32(&sh->vst_full[i]), 1);
-      mbar_init(smem_u32(&sh->vst_empty[i]), kVConvThreads);
+      mbar_init(smem_u32(&sh->vst_empty[i]), kVConvThreads / 32);
     }
     for (int i = 0; i < kScSlots; ++i) {
-      mbar_init(smem_u32(&sh->sc_full[i]), 32);
-      mbar_init(smem_u32(&sh->sc_free[i]), kSoftmaxThreads / 2);
+      mbar_init(smem_u32(&sh->sc_full[i]), 128);
+      mbar_init(smem_u32(&sh->sc_free[i]), kSoftmaxWarps);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&sh->s_full[i]), 1);
-      mbar_init(smem_u32(&sh->s_free[i]), kSoftmaxThreads);
-      mbar_init(smem_u32(&sh->p_full[i]), kSoftmaxThreads / 2);
+      mbar_init(smem_u32(&sh->s_free[i]), kSoftmaxWarps);
+      mbar_init(smem_u32(&sh->p_full[i]), kSoftmaxWarps / 2);
       mbar_init(smem_u32(&sh->p_free[i]), 1);
-      mbar_init(smem_u32(&sh->vt_full[i]), kVConvThreads);
-      mbar_init(smem_u32(&sh->vt_free[i]), 1);
       mbar_init(smem_u32(&sh->o_done[i]), 1);
     }
-    mbar_init(smem_u32(&sh->o_free), kSoftmaxThreads);
-    mbar_init(smem_u32(&sh->q_full), kSoftmaxThreads);
-    mbar_init(smem_u32(&sh->smx), kSoftmaxThreads);
+    for (int i = 0; i < kVtBufs; ++i) {
+      mbar_init(smem_u32(&sh->vt_full[i]), kVConvThreads / 32);
+      mbar_init(smem_u32(&sh->vt_free[i]), 1);
+    }
+    mbar_init(smem_u32(&sh->o_free), kSoftmaxWarps);
+    mbar_init(smem_u32(&sh->q_full), kSoftmaxWarps);
+    mbar_init(smem_u32(&sh->smx), kSoftmaxWarps);
     mbar_init(smem_u32(&sh->drain), 1);
     sh->abort_flag = 0;
     rd->slow_tile[0] = rd->slow_tile[1] = -1;
@@ -330,7 +334,11 @@ verify_tt_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmap) {
   SegIter iter{stp, seq_T, seq_ctx, B, G, Hkv, window, tile_begin(blockIdx.x, total, ncta),
                tile_begin(blockIdx.x + 1, total, ncta)};
 
+  // Register split: the softmax warpgroups (warps 0-7) take 160 registers a
+  // thread, the converter / MMA warpgroups 96: 256 x 160 + 256 x 96 = 65536,
+  // the launch's 512 x 128. Each warpgroup changes its share uniformly.
   if (warp < kSoftmaxWarps) {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 160;" ::: "memory");
     // ===================================================== softmax + epilogue
     const int q = warp & 3, part = warp >> 2, st = tid;
     const int cb = 48 * part;                             // first column (row) of this thread
@@ -341,8 +349,8 @@ verify_tt_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmap) {
     Seg s;
     bool ok = true;
     auto smx_sync = [&]() -> bool {
-      mbar_arrive(smx);
-      const bool r = sync.wait(smx, sbp & 1);
+      warp_arrive(smx, lane);
+      const bool r = __all_sync(0xffffffffu, sync.wait(smx, sbp & 1));
       ++sbp;
       return r;
     };
@@ -402,7 +410,7 @@ verify_tt_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmap) {
         }
         if (st < 128) rd->m[st] = kMInit;
         fence_async_smem();
-        mbar_arrive(smem_u32(&sh->q_full));
+        warp_arrive(smem_u32(&sh->q_full), lane);
         ok = smx_sync();
         if (!ok) break;
       }
@@ -413,18 +421,18 @@ verify_tt_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmap) {
       for (int i = 0; i < 48; ++i) lsum[i] = 0.f;
 
       for (int it = s.i0; it < s.i1 && ok; ++it, ++g) {
-        const int sub = 2 * g + (q >> 1);                 // sub-stage of this thread's key
-        const int ssl = sub % kScSlots;
-        ok = sync.wait(smem_u32(&sh->sc_full[ssl]), (sub / kScSlots) & 1) &&
+        const int ssl = g % kScSlots;
+        ok = sync.wait(smem_u32(&sh->sc_full[ssl]), (g / kScSlots) & 1) &&
              sync.wait(smem_u32(&sh->s_full[g & 1]), (g >> 1) & 1);
+        ok = __all_sync(0xffffffffu, ok);       // a timeout seen by some lanes stops the warp
         if (!ok) break;
         fence_after();
         const int j = it * kTileKeys + 32 * q + lane;     // this thread's key
         const bool kvalid = j < s.Lk && j >= (s.klo & ~(kPageSize - 1));
-        const float* sc = scales + ssl * 2 * kSubKeys;
-        const float ksc = kvalid ? sc[kl] : 0.f;
-        const float vsc = kvalid ? sc[kSubKeys + kl] : 0.f;
-        mbar_arrive(smem_u32(&sh->sc_free[ssl]));
+        const float* sc = scales + ssl * 2 * kTileKeys;
+        const float ksc = kvalid ? sc[32 * q + lane] : 0.f;
+        const float vsc = kvalid ? sc[kTileKeys + 32 * q + lane] : 0.f;
+        warp_arrive(smem_u32(&sh->sc_free[ssl]), lane);
         // rows that see key j: t >= j - ctx (and t < j - ctx + W with a window)
         int c_lo = R, c_hi = 0;
         if (kvalid) {
@@ -437,14 +445,11 @@ verify_tt_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmap) {
         const float lv = __log2f(vsc);                    // -inf for a zero (or untrusted) scale
         const uint32_t s_addr = tmem + lane_off + kColS + (uint32_t)((g & 1) * kNMax + cb);
 
-        // ---- pass 1: does any visible key break its row's bounds?
+        // ---- pass 1: does any visible key break its row's bounds? (the
+        // TMEM load of the next 16 columns is in flight while one is checked)
         float tmx = -INFINITY;
         if (live) {
-#pragma unroll
-          for (int k = 0; k < 3; ++k) {
-            uint32_t sv[16];
-            tmem_ld32x32b_x16(s_addr + 16 * k, sv);
-            tmem_wait_ld();
+          auto check = [&](const uint32_t (&sv)[16], int k) {
             const float4* mp = reinterpret_cast<const float4*>(rd->m + cb + 16 * k);
 #pragma unroll
             for (int i4 = 0; i4 < 4; ++i4) {
@@ -458,7 +463,17 @@ verify_tt_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmap) {
                 tmx = fmaxf(tmx, x);
               }
             }
-          }
+          };
+          uint32_t sa[16], sb[16];
+          tmem_ld32x32b_x16(s_addr, sa);
+          tmem_wait_ld(sa);
+          tmem_ld32x32b_x16(s_addr + 16, sb);
+          check(sa, 0);
+          tmem_wait_ld(sb);
+          tmem_ld32x32b_x16(s_addr + 32, sa);
+          check(sb, 1);
+          tmem_wait_ld(sa);
+          check(sa, 2);
         }
         const bool need = tmx + lv > kPLimit || tmx > kWLimit;
         if (__any_sync(0xffffffffu, need) && lane == 0) rd->slow_tile[g & 1] = g;
@@ -473,7 +488,7 @@ verify_tt_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmap) {
             if (live) {
               uint32_t sv[16];
               tmem_ld32x32b_x16(s_addr + 16 * k, sv);
-              tmem_wait_ld();
+              tmem_wait_ld(sv);
 #pragma unroll
               for (int i = 0; i < 16; ++i) {
                 const int c = cb + 16 * k + i;
@@ -502,7 +517,7 @@ verify_tt_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmap) {
           if (!ok) break;
           if (it > s.i0) {
             // O^T holds the tiles before this one: rescale once their PVs are done
-            ok = sync.wait(smem_u32(&sh->o_done[(g - 1) & 1]), ((g - 1) >> 1) & 1);
+            ok = __all_sync(0xffffffffu, sync.wait(smem_u32(&sh->o_done[(g - 1) & 1]), ((g - 1) >> 1) & 1));
             if (!ok) break;
             fence_after();
 #pragma unroll 1
@@ -510,7 +525,7 @@ verify_tt_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmap) {
               uint32_t v[32];
               const uint32_t oa = tmem + lane_off + kColO + (uint32_t)(part * kNMax + c0);
               tmem_ld32x32b_x32(oa, v);
-              tmem_wait_ld();
+              tmem_wait_ld(v);
 #pragma unroll
               for (int i = 0; i < 32; ++i)
                 v[i] = __float_as_uint(__uint_as_float(v[i]) * rd->alpha[c0 + i]);
@@ -526,17 +541,14 @@ verify_tt_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmap) {
         // P^T half q/2 is free once the PVs of the previous tile that read it
         // are done (normally long before: they were issued a tile ago).
         if (g > 0) {
-          ok = sync.wait(smem_u32(&sh->p_free[q >> 1]), (g - 1) & 1);
+          ok = __all_sync(0xffffffffu, sync.wait(smem_u32(&sh->p_free[q >> 1]), (g - 1) & 1));
           if (!ok) break;
         }
         const float vsv = vsc;                            // 0 for keys outside the pages
         if (live) {
           uint8_t* pd = pbuf + (q >> 1) * kPHalfBytes + kl * 128;
-#pragma unroll
-          for (int k = 0; k < 3; ++k) {
-            uint32_t sv[16], pk[8];
-            tmem_ld32x32b_x16(s_addr + 16 * k, sv);
-            tmem_wait_ld();
+          auto emit = [&](const uint32_t (&sv)[16], int k) {
+            uint32_t pk[8];
             const float4* mp = reinterpret_cast<const float4*>(rd->m + cb + 16 * k);
 #pragma unroll
             for (int i4 = 0; i4 < 4; ++i4) {
@@ -563,12 +575,22 @@ verify_tt_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmap) {
               *reinterpret_cast<uint4*>(pd + (r0 >> 6) * kPAtom + ((((r0 & 63) >> 3) ^ (kl & 7)) << 4)) =
                   make_uint4(pk[4 * hh], pk[4 * hh + 1], pk[4 * hh + 2], pk[4 * hh + 3]);
             }
-          }
+          };
+          uint32_t sa[16], sb[16];
+          tmem_ld32x32b_x16(s_addr, sa);
+          tmem_wait_ld(sa);
+          tmem_ld32x32b_x16(s_addr + 16, sb);
+          emit(sa, 0);
+          tmem_wait_ld(sb);
+          tmem_ld32x32b_x16(s_addr + 32, sa);
+          emit(sb, 1);
+          tmem_wait_ld(sa);
+          emit(sa, 2);
         }
         fence_before();
-        mbar_arrive(smem_u32(&sh->s_free[g & 1]));
+        warp_arrive(smem_u32(&sh->s_free[g & 1]), lane);
         fence_async_smem();
-        mbar_arrive(smem_u32(&sh->p_full[q >> 1]));
+        warp_arrive(smem_u32(&sh->p_full[q >> 1]), lane);
       }
       if (!ok) break;
 
@@ -594,7 +616,8 @@ verify_tt_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmap) {
         if (ns == 1) p.lse[(size_t)(q_off[s.b] + t) * p.num_q_heads + s.h * G + gg] = lse;
         else lse_part[prow0 + c] = lse;
       }
-      ok = smx_sync() && sync.wait(smem_u32(&sh->o_done[(g - 1) & 1]), ((g - 1) >> 1) & 1);
+      ok = smx_sync() &&
+           __all_sync(0xffffffffu, sync.wait(smem_u32(&sh->o_done[(g - 1) & 1]), ((g - 1) >> 1) & 1));
       if (!ok) break;
       fence_after();
       {
@@ -604,7 +627,7 @@ verify_tt_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmap) {
         for (int c0 = 0; c0 < R; c0 += 16) {
           uint32_t v[16];
           tmem_ld32x32b_x16(tmem + lane_off + kColO + (uint32_t)(part * kNMax + c0), v);
-          tmem_wait_ld();
+          tmem_wait_ld(v);
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const int c = c0 + i;
@@ -624,9 +647,10 @@ verify_tt_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmap) {
         }
       }
       fence_before();
-      mbar_arrive(smem_u32(&sh->o_free));
+      warp_arrive(smem_u32(&sh->o_free), lane);
     }
   } else if (warp < kVConvWarp0) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 96;" ::: "memory");
     // ============================================================ K converters
     const int q = warp - kKConvWarp0;
     const uint32_t lane_off = (uint32_t)(32 * q) << 16;
@@ -636,13 +660,17 @@ verify_tt_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmap) {
     Seg cs;
     int c_it = 0, c_end = 0, issued = 0;
     PageWindow win;
-    auto issue_next = [&]() {
+    auto issue_next = [&]() -> bool {
       if (c_it >= c_end) {
-        if (!cit.next(cs)) return;
+        if (!cit.next(cs)) return true;
         c_it = cs.i0;
         c_end = cs.i1;
       }
-      const int slot = issued % kKDepth;
+      const int slot = issued % kKDepth, ssl = issued % kScSlots;
+      // the scale slot is free once the softmax is done with tile issued - kScSlots
+      bool okk = true;
+      if (lane == 0) okk = sync.wait(smem_u32(&sh->sc_free[ssl]), ((issued / kScSlots) & 1) ^ 1);
+      if (!__shfl_sync(0xffffffffu, okk, 0)) return false;
       const uint32_t bar = smem_u32(&sh->kst_full[q][slot]);
       const int first = (c_it * kTileKeys + 32 * q) / kPageSize;       // this warp's 2 pages
       const int npages = (cs.Lk + kPageSize - 1) / kPageSize;
@@ -654,19 +682,28 @@ verify_tt_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmap) {
       if (page >= 0)
         tensor_g2s_3d(smem_u32(mystage + slot * kKStage + lane * kPageBytes), &tmap, 0,
                       (page * Hkv + cs.h) * 2 * kPageSize, 0, bar);
+      // K / V scales of the two pages: lanes 0-7 K, 8-15 V; page (lane >> 2) & 1
+      const int which = (lane >> 3) & 1, pg = (lane >> 2) & 1, ch = lane & 3;
+      const int ps = __shfl_sync(0xffffffffu, page, pg);
+      if (lane < 16 && ps >= 0)
+        cp_async16(smem_u32(scales + ssl * 2 * kTileKeys + which * kTileKeys + 32 * q + 16 * pg + 4 * ch),
+                   (which ? p.v_scales : p.k_scales) + ((size_t)ps * Hkv + cs.h) * kPageSize + 4 * ch);
+      cp_async_arrive_noinc(smem_u32(&sh->sc_full[ssl]));
       ++c_it;
       ++issued;
+      return true;
     };
-    for (int d = 0; d < kKDepth; ++d) issue_next();
+    bool ok = true;
+    for (int d = 0; d < kKDepth && ok; ++d) ok = issue_next();
     int g = 0;
     Seg s;
-    bool ok = true;
     const int slot_row = lane & 15;
     while (ok && iter.next(s)) {
-      for (int it = s.i0; it < s.i1; ++it, ++g) {
+      for (int it = s.i0; it < s.i1 && ok; ++it, ++g) {
         const int slot = g % kKDepth;
         ok = sync.wait(smem_u32(&sh->kst_full[q][slot]), (g / kKDepth) & 1) &&
              (g == 0 || sync.wait(smem_u32(&sh->kt_free), (g - 1) & 1));
+        ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         fence_after();
         const uint8_t* row = mystage + slot * kKStage + (lane >> 4) * kPageBytes + slot_row * 128;
@@ -688,54 +725,111 @@ verify_tt_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmap) {
         }
         tmem_wait_st();
         fence_before();
-        mbar_arrive(smem_u32(&sh->kt_full));
+        warp_arrive(smem_u32(&sh->kt_full), lane);
         __syncwarp();                                     // the stage is read: refill it
-        issue_next();
+        ok = issue_next();
       }
     }
     // copies still in flight (only after an abort) land before the CTA exits
     if (lane == 0)
       for (int t = g; t < issued; ++t)
         sync.drain(smem_u32(&sh->kst_full[q][t % kKDepth]), (t / kKDepth) & 1);
-  } else if (warp < kMmaWarp) {
+    asm volatile("cp.async.wait_all;" ::: "memory");
+  } else {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 96;" ::: "memory");
+    if (warp != kMmaWarp) {
     // ============================================================ V converters
-    const int tv = tid - 32 * kVConvWarp0;
-    const int kloc = 8 * ((tv >> 3) & 3) + (tv & 7);     // key within the 32-key buffer
+    const int tv = (warp == 15 ? 64 : 32 * (warp - kVConvWarp0)) + lane;
+    const bool issuer = warp == kVConvWarp0;            // also issues the V copies
+    SegIter vit = iter;
+    Seg cs;
+    int v_it = 0, v_end = 0, v_hh = 0, vissued = 0;
+    PageWindow win;
+    // V codes of the next 64-key stage into slot vissued % kVRing
+    auto issue_v = [&]() {
+      if (v_hh == 0 && v_it >= v_end) {
+        if (!vit.next(cs)) return;
+        v_it = cs.i0;
+        v_end = cs.i1;
+      }
+      const int slot = vissued % kVRing;
+      const uint32_t bar = smem_u32(&sh->vst_full[slot]);
+      const int first = (v_it * kTileKeys + v_hh * kSubKeys) / kPageSize;
+      const int npages = (cs.Lk + kPageSize - 1) / kPageSize;
+      const int id = win.get(p, cs.b, first, npages, lane);
+      const int page = needed_page(p, cs, first, lane < 4, id, lane);
+      const unsigned mask = __ballot_sync(0xffffffffu, page >= 0) & 15u;
+      if (lane == 0) mbar_expect_tx(bar, (uint32_t)__popc(mask) * kPageBytes);
+      __syncwarp();
+      if (page >= 0)
+        tensor_g2s_3d(smem_u32(vst + slot * kVStage + lane * kPageBytes), &tmap, 0,
+                      (page * Hkv + cs.h) * 2 * kPageSize + kPageSize, 0, bar);
+      if (++v_hh == 2) {
+        v_hh = 0;
+        ++v_it;
+      }
+      ++vissued;
+    };
+    if (issuer)
+      for (int i = 0; i < kVRing; ++i) issue_v();
     int g = 0;
     Seg s;
     bool ok = true;
     while (ok && iter.next(s)) {
       for (int it = s.i0; it < s.i1 && ok; ++it, ++g) {
-        for (int qq = 0; qq < 4; ++qq) {
-          const int gq = 4 * g + qq, sub = 2 * g + (qq >> 1), vs = sub % kVRing;
-          ok = ((qq & 1) || sync.wait(smem_u32(&sh->vst_full[vs]), (sub / kVRing) & 1)) &&
-               sync.wait(smem_u32(&sh->vt_free[gq & 1]), ((gq >> 1) & 1) ^ 1);
+        for (int c = 0; c < kTileKeys / kVtKeys; ++c) {
+          const int gc = 8 * g + c, sub = 2 * g + (c >> 2), vs = sub % kVRing, vb = gc % kVtBufs;
+          ok = ((c & 3) || sync.wait(smem_u32(&sh->vst_full[vs]), (sub / kVRing) & 1)) &&
+               sync.wait(smem_u32(&sh->vt_free[vb]), ((gc / kVtBufs) & 1) ^ 1);
+          ok = __all_sync(0xffffffffu, ok);
           if (!ok) break;
-          const int key = 32 * (qq & 1) + kloc, pg = key >> 4, sl = key & 15;
-          const uint8_t* src = vst + vs * kVStage + pg * kPageBytes + sl * 128;
-          uint8_t* dst = vtb + (gq & 1) * kVtBytes + kloc * 128;
+          uint8_t* dstb = vtb + vb * kVtBytes;
+          const uint8_t* srcb = vst + vs * kVStage + (c & 3) * kPageBytes;   // page c & 3 of the stage
+          // job j: key (slot) j & 15, 16-byte chunk j >> 4 of its row; a
+          // quarter warp takes 8 consecutive keys of one chunk: its loads and
+          // stores fall in 8 distinct bank groups (both layouts swizzle by key & 7)
 #pragma unroll
-          for (int i8 = 0; i8 < 8; ++i8) {
-            const int hc = (tv >> 5) + 2 * i8, hh = hc >> 3, c = hc & 7;
-            const uint4 w = *reinterpret_cast<const uint4*>(src + hh * kPageHalf + ((c ^ (sl & 7)) << 4));
-            uint4 h0, h1;
-            i8x4_to_h2x2(w.x, h0.x, h0.y);
-            i8x4_to_h2x2(w.y, h0.z, h0.w);
-            i8x4_to_h2x2(w.z, h1.x, h1.y);
-            i8x4_to_h2x2(w.w, h1.z, h1.w);
-            uint8_t* da = dst + (2 * hh + (c >> 2)) * kVtAtom;
-            const int e0 = 2 * (c & 3);
-            *reinterpret_cast<uint4*>(da + ((e0 ^ (kloc & 7)) << 4)) = h0;
-            *reinterpret_cast<uint4*>(da + (((e0 + 1) ^ (kloc & 7)) << 4)) = h1;
+          for (int i = 0; i < 3; ++i) {
+            const int jb = tv + kVConvThreads * i;
+            if (jb < kVtKeys * 16) {
+              const int kloc = jb & 15, hc = jb >> 4, hh = hc >> 3, cc = hc & 7;
+              const uint4 w = *reinterpret_cast<const uint4*>(
+                  srcb + hh * kPageHalf + kloc * 128 + ((cc ^ (kloc & 7)) << 4));
+              uint4 h0, h1;
+              i8x4_to_h2x2(w.x, h0.x, h0.y);
+              i8x4_to_h2x2(w.y, h0.z, h0.w);
+              i8x4_to_h2x2(w.z, h1.x, h1.y);
+              i8x4_to_h2x2(w.w, h1.z, h1.w);
+              uint8_t* da = dstb + (2 * hh + (cc >> 2)) * kVtAtom + kloc * 128;
+              const int e0 = 2 * (cc & 3);
+              *reinterpret_cast<uint4*>(da + ((e0 ^ (kloc & 7)) << 4)) = h0;
+              *reinterpret_cast<uint4*>(da + (((e0 + 1) ^ (kloc & 7)) << 4)) = h1;
+            }
           }
           fence_async_smem();
-          mbar_arrive(smem_u32(&sh->vt_full[gq & 1]));
-          if (qq & 1) mbar_arrive(smem_u32(&sh->vst_empty[vs]));
+          warp_arrive(smem_u32(&sh->vt_full[vb]), lane);
+          if ((c & 3) == 3) {
+            warp_arrive(smem_u32(&sh->vst_empty[vs]), lane);
+            if (issuer) {                               // refill the stage once all have read it
+              bool okk = true;
+              if (lane == 0) okk = sync.wait(smem_u32(&sh->vst_empty[vs]), (sub / kVRing) & 1);
+              ok = __shfl_sync(0xffffffffu, okk, 0);
+              if (!ok) break;
+              issue_v();
+            }
+          }
         }
       }
     }
-  } else if (warp == kMmaWarp) {
-    // ============================================================ MMA issue
+    // V copies in flight after an abort land before the CTA exits (a stage is
+    // re-armed only after its previous copies were consumed)
+    if (issuer && lane == 0)
+      for (int r = 0; r < kVRing && r < vissued; ++r) {
+        const int last = r + ((vissued - 1 - r) / kVRing) * kVRing;
+        sync.drain(smem_u32(&sh->vst_full[r]), (last / kVRing) & 1);
+      }
+    } else {
+    // ============================================================ MMA issue (warp 14)
     if (lane == 0) {
       const uint64_t qdesc0 = sdesc(smem_u32(qbuf), 16, 1024);
       const uint64_t vtdesc0 = sdesc(smem_u32(vtb), kVtAtom, 1024);
@@ -744,7 +838,7 @@ verify_tt_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmap) {
       Seg qs, ps;
       bool qk_more = qi.next(qs), pv_more = pi.next(ps);
       int qk_tile = qk_more ? qs.i0 : 0, g_qk = 0, seg_qk = 0;
-      int pv_tile = pv_more ? ps.i0 : 0, g_pv = 0, qq = 0, seg_pv = 0;
+      int pv_tile = pv_more ? ps.i0 : 0, g_pv = 0, ck = 0, seg_pv = 0;
       bool q_ready = false, pv_first = true;
       uint32_t idq = idesc_f16(128, (qs.R + 15) & ~15, 0, 0);
       uint32_t idp = idesc_f16(128, (ps.R + 15) & ~15, 1, 1);
@@ -778,26 +872,23 @@ verify_tt_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmap) {
           }
         }
         if (pv_more && g_pv < g_qk) {
-          const int gq = 4 * g_pv + qq;
-          bool rdy = mbar_test_wait(smem_u32(&sh->p_full[qq >> 1]), g_pv & 1) &&
-                     mbar_test_wait(smem_u32(&sh->vt_full[gq & 1]), (gq >> 1) & 1);
-          if (rdy && pv_first && qq == 0 && seg_pv > 0)
+          const int gc = 8 * g_pv + ck, vb = gc % kVtBufs;
+          bool rdy = mbar_test_wait(smem_u32(&sh->p_full[ck >> 2]), g_pv & 1) &&
+                     mbar_test_wait(smem_u32(&sh->vt_full[vb]), (gc / kVtBufs) & 1);
+          if (rdy && pv_first && ck == 0 && seg_pv > 0)
             rdy = mbar_test_wait(smem_u32(&sh->o_free), (seg_pv - 1) & 1);
           if (rdy) {
             fence_after();
-#pragma unroll
-            for (int dh = 0; dh < 2; ++dh)
-#pragma unroll
-              for (int ks = 0; ks < 2; ++ks)
-                mma_ss(tmem + kColO + (uint32_t)(dh * kNMax),
-                       vtdesc0 + (uint64_t)(((gq & 1) * kVtBytes + dh * 2 * kVtAtom + ks * 2048) >> 4),
-                       pdesc0 + (uint64_t)(((qq >> 1) * kPHalfBytes + (qq & 1) * 4096 + ks * 2048) >> 4),
-                       idp, (pv_first && qq == 0 && ks == 0) ? 0u : 1u);
-            mma_commit(smem_u32(&sh->vt_free[gq & 1]));
-            if (qq & 1) mma_commit(smem_u32(&sh->p_free[qq >> 1]));
-            if (qq == 3) mma_commit(smem_u32(&sh->o_done[g_pv & 1]));
-            if (++qq == 4) {
-              qq = 0;
+            const uint64_t pdesc = pdesc0 + (uint64_t)(((ck >> 2) * kPHalfBytes + (ck & 3) * 2048) >> 4);
+            const uint64_t vdesc = vtdesc0 + (uint64_t)((vb * kVtBytes) >> 4);
+            const uint32_t acc = (pv_first && ck == 0) ? 0u : 1u;
+            mma_ss(tmem + kColO, vdesc, pdesc, idp, acc);
+            mma_ss(tmem + kColO + kNMax, vdesc + (uint64_t)((2 * kVtAtom) >> 4), pdesc, idp, acc);
+            mma_commit(smem_u32(&sh->vt_free[vb]));
+            if ((ck & 3) == 3) mma_commit(smem_u32(&sh->p_free[ck >> 2]));
+            if (ck == 7) mma_commit(smem_u32(&sh->o_done[g_pv & 1]));
+            if (++ck == kTileKeys / kVtKeys) {
+              ck = 0;
               pv_first = false;
               ++g_pv;
               if (++pv_tile == ps.i1) {
@@ -828,54 +919,7 @@ verify_tt_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmap) {
       sync.drain(smem_u32(&sh->drain), 0);
     }
     __syncwarp();
-  } else {
-    // ============================================================ producer
-    int gsub = 0;
-    Seg s;
-    bool ok = true;
-    PageWindow win;
-    while (ok && iter.next(s)) {
-      const int npages = (s.Lk + kPageSize - 1) / kPageSize;
-      for (int it = s.i0; it < s.i1 && ok; ++it) {
-        for (int hh = 0; hh < 2; ++hh, ++gsub) {
-          const int vs = gsub % kVRing, ssl = gsub % kScSlots;
-          if (lane == 0)
-            ok = sync.wait(smem_u32(&sh->vst_empty[vs]), ((gsub / kVRing) & 1) ^ 1) &&
-                 sync.wait(smem_u32(&sh->sc_free[ssl]), ((gsub / kScSlots) & 1) ^ 1);
-          ok = __shfl_sync(0xffffffffu, ok, 0);
-          if (!ok) break;
-          const int first = (it * kTileKeys + hh * kSubKeys) / kPageSize;
-          const int id = win.get(p, s.b, first, npages, lane);
-          const int page = needed_page(p, s, first, lane < 4, id, lane);
-          const uint32_t bar = smem_u32(&sh->vst_full[vs]);
-          const unsigned mask = __ballot_sync(0xffffffffu, page >= 0) & 15u;
-          if (lane == 0) mbar_expect_tx(bar, (uint32_t)__popc(mask) * kPageBytes);
-          __syncwarp();
-          if (page >= 0)
-            tensor_g2s_3d(smem_u32(vst + vs * kVStage + lane * kPageBytes), &tmap, 0,
-                          (page * Hkv + s.h) * 2 * kPageSize + kPageSize, 0, bar);
-          // scales: lanes 0-15 K, 16-31 V; page (lane & 15) / 4, slots 4 * (lane & 3)..
-          const int sj = (lane & 15) >> 2;
-          const int ps = __shfl_sync(0xffffffffu, page, sj);
-          if (ps >= 0) {
-            const float* src = (lane < 16 ? p.k_scales : p.v_scales) +
-                               ((size_t)ps * Hkv + s.h) * kPageSize + 4 * (lane & 3);
-            cp_async16(smem_u32(scales + ssl * 2 * kSubKeys + (lane < 16 ? 0 : kSubKeys) +
-                                sj * kPageSize + 4 * (lane & 3)),
-                       src);
-          }
-          cp_async_arrive_noinc(smem_u32(&sh->sc_full[ssl]));
-        }
-      }
     }
-    // V copies in flight after an abort land before the CTA exits (a stage is
-    // re-armed only after its previous copies were consumed)
-    if (lane == 0)
-      for (int r = 0; r < kVRing && r < gsub; ++r) {
-        const int last = r + ((gsub - 1 - r) / kVRing) * kVRing;
-        sync.drain(smem_u32(&sh->vst_full[r]), (last / kVRing) & 1);
-      }
-    asm volatile("cp.async.wait_all;" ::: "memory");
   }
 
   fence_before();
