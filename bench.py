@@ -1,21 +1,33 @@
 #!/usr/bin/env python3
-"""Benchmark: verify attention over an int8 paged KV cache on one GB300.
+"""Benchmark: verify attention over an int8 paged KV cache on GB300.
 
 One step = one pass of the whole hot path over the workload's batch:
 ``splash_kv_append`` of every sequence's verify block (quantise + scatter),
-then ``splash_verify_attention`` (split planner, attention kernels, log-sum-exp
+then ``splash_verify_attention`` (split planner, attention kernel, log-sum-exp
 combine). Default workload: 16 sequences x 32768 cached tokens, 24 query / 4
-KV heads, head_dim 256, T = 16, int8 KV with 1% outlier channels. The KV cache
-(1.09 GB) is larger than L2 (129 MB), so no flush is needed between steps.
+KV heads, head_dim 256, T = 16, int8 KV with 1% outlier channels.
 
-Prints one JSON line. ``--impl reference`` times the fp64 CPU oracle (the
-reference arm: a slow, plain program) on a bounded sample of the same workload.
+Timing: W warm-up steps, then the GPU is kept busy for at least 2 s of steps
+(nvidia-smi samples the clocks over that window and the timed region that
+follows), then exactly K timed steps between a barrier and a synchronize,
+CUDA events on the launching stream, max over ranks. Inputs that L2 could
+hold (a pool under 2 x L2) are rotated over enough identical pool copies
+that each step reads a pool the previous steps did not leave in L2.
+
+With N ranks (one GPU each, torchrun; ``--gpus N`` re-launches itself under
+torchrun) the seeded batch is partitioned across ranks, balanced by KV bytes;
+no data moves between ranks, only the timing reduction (strong scaling: the
+batch is fixed). Prints one JSON line. ``--impl reference`` times the fp64
+CPU oracle (the reference arm: a slow, plain program) on a bounded sample of
+the same workload.
 """
 from __future__ import annotations
 
 import argparse
 import json
+import math
 import os
+import socket
 import statistics
 import subprocess
 import sys
@@ -33,6 +45,8 @@ METRIC = "verify tokens/s and achieved HBM GB/s (% of GB300 peak), 16×32K int8 
 UNIT = "verify tokens/s"
 DEFAULT_WORKLOAD = "batch16_32k"
 FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 10 ** 6                 # GB300 L2
+CLOCK_WINDOW_S = 2.0                     # sustained load around the timed region
 
 
 def parse_args(argv=None):
@@ -42,24 +56,22 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=[s.name for s in wl.SPECS])
-    ap.add_argument("--path", type=int, default=0, help="0 auto, 1 CUDA-core, 2 tensor-core")
+    ap.add_argument("--path", type=int, default=0,
+                    help="0 auto, 1 CUDA-core, 2 tensor-core, 3 transposed tensor-core")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--oracle-sample", type=float, default=0.0, help=argparse.SUPPRESS)
     return ap.parse_args(argv)
 
 
-# ---- multi-rank plumbing (weak scaling: every rank runs its own batch) ------
+# ---- multi-rank plumbing ------------------------------------------------------
 def rank_info():
     return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
             int(os.environ.get("LOCAL_RANK", "0")))
 
 
-def rank_seed(spec: wl.WorkloadSpec, rank: int) -> int:
-    """Each rank draws an independent batch of the same shape."""
-    return spec.seed + 7919 * rank
-
-
 def reduce_max(value: float, world: int, device=None) -> float:
+    """Max over ranks (a CUDA tensor under NCCL, a CPU tensor under gloo)."""
     if world == 1:
         return value
     import torch
@@ -75,6 +87,28 @@ def barrier(world: int):
         dist.barrier()
 
 
+def rank_sequences(W: wl.Workload, world: int, rank: int):
+    """This rank's share of the batch: KV-byte balanced partition."""
+    if world == 1:
+        return list(range(W.num_seqs))
+    return wl.partition_by_kv_bytes(W, world)[rank]
+
+
+def free_port() -> int:
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def relaunch_under_torchrun(args) -> int:
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+           f"--nproc-per-node={args.gpus}", "--master-addr", "127.0.0.1",
+           f"--master-port={free_port()}", os.path.abspath(__file__), *sys.argv[1:]]
+    return subprocess.call(cmd)
+
+
 # ---- peaks, clocks, profiles -------------------------------------------------
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -87,7 +121,7 @@ def load_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi sampling during the timed region."""
+    """nvidia-smi samples (every 100 ms) of the SM clock and throttle reasons."""
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -117,12 +151,13 @@ class ClockSampler:
             self.proc.kill()
         self.file.seek(0)
         rows = [r.split(",") for r in self.file.read().strip().splitlines() if r.strip()]
-        sm, mx, reasons = [], 0.0, set()
+        sm, mx, reasons, power = [], 0.0, set(), []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for r in rows:
             try:
                 sm.append(float(r[0]))
                 mx = max(mx, float(r[1]))
+                power.append(float(r[2]))
                 for n, v in zip(names, r[4:8]):
                     if v.strip().lower() == "active":
                         reasons.add(n)
@@ -131,7 +166,9 @@ class ClockSampler:
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "power_w_median": statistics.median(power) if power else None,
+                "window": f"{CLOCK_WINDOW_S:.0f} s or more of back-to-back steps ending with the "
+                          "timed region"}
 
 
 def kernel_traffic(kernel: str, workload: str):
@@ -155,6 +192,9 @@ def kernel_traffic(kernel: str, workload: str):
 
 # ---- CPU baseline: the fp64 oracle on a bounded sample ----------------------
 def oracle_threads() -> int:
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(var, "").isdigit():
+            return int(os.environ[var])
     try:
         from threadpoolctl import threadpool_info
         n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
@@ -208,6 +248,20 @@ def cpu_baseline(W: wl.Workload, budget_s: float, max_steps: int | None = None):
                       f"{elapsed:.1f} s of fp64 numpy"}, elapsed, tokens
 
 
+def cpu_baseline_one_core(workload: str, budget_s: float):
+    """The same sample timed in a child process whose BLAS / OpenMP use one thread."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    for var in ("RANK", "WORLD_SIZE", "LOCAL_RANK"):
+        env.pop(var, None)
+    try:
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--workload", workload,
+                            "--oracle-sample", str(budget_s)],
+                           env=env, capture_output=True, text=True, timeout=600)
+        return json.loads(r.stdout.strip().splitlines()[-1])
+    except (subprocess.SubprocessError, ValueError, IndexError):
+        return None
+
+
 def run_reference(args):
     rank, world, _ = rank_info()
     if rank != 0:
@@ -224,7 +278,7 @@ def run_reference(args):
     value = tot_tok / tot_t
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot_t / args.steps,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "higher_is_better": True, "scaling": "strong", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded; stands in for the pages' coding prompts)",
             "config": {"workload": W.spec.name, "seqs": W.num_seqs,
                        "sample": "one sequence per step"},
@@ -236,58 +290,91 @@ def run_reference(args):
 
 
 # ---- GPU arm -------------------------------------------------------------------
+def pool_copies_for(pool_bytes: int) -> int:
+    """Identical pools to rotate over so that consecutive steps read more than
+    2 x L2 of distinct pool bytes (1 when one pool already exceeds that)."""
+    if pool_bytes >= 2 * L2_BYTES:
+        return 1
+    return min(8, math.ceil(2 * L2_BYTES / max(pool_bytes, 1)))
+
+
 def run_ours(args):
     import torch
     rank, world, local = rank_info()
     if world > 1:
         import torch.distributed as dist
-        dist.init_process_group("nccl")
-    torch.cuda.set_device(local)
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     from speculative_verify_attention_kv_gb300 import splash_kv as sk
     from speculative_verify_attention_kv_gb300.device_workload import DeviceWorkload
 
-    spec = wl.SPEC_BY_NAME[args.workload]
-    W = wl.Workload(spec, rank_seed(spec, rank))
+    dev = torch.device("cuda", torch.cuda.current_device())
+    W_full = wl.make(args.workload)
+    W = W_full.subset(rank_sequences(W_full, world, rank)) if world > 1 else W_full
     dw = DeviceWorkload(W)
+    n_copies = pool_copies_for(dw.pool_bytes())
+    dw.add_pool_copies(n_copies)
     stream = torch.cuda.current_stream()
-    n_tok = W.num_q_tokens
     algo_bytes = W.algorithmic_bytes()
+    has_work = W.num_q_tokens > 0
 
-    ev_a0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ev_a1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev_c = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
 
-    def step(i=None):
+    def step(i, timed_k=None):
+        """Step on pool copy i; timed_k: index of the timed step (events)."""
+        dw.use_pool(i)
+        if not has_work:
+            return
         dw.append_block()
-        ev = (ev_a0[i], ev_a1[i]) if i is not None else None
+        ev = (ev_b[timed_k], ev_a[timed_k]) if timed_k is not None else None
         sk.splash_verify_attention(dw.q, *dw.pool, dw.table, dw.ctx, dw.T, float(W.sm_scale),
                                    dw.max_T, dw.out, dw.lse, dw.ws, device_status=dw.status,
                                    path=args.path, events=ev)
+        if timed_k is not None:
+            ev_c[timed_k].record(stream)   # after the log-sum-exp combine
 
-    for e in ev_a0 + ev_a1:      # creates the events; the library re-records them
+    for e in ev_b + ev_a + ev_c:      # creates the events; the library re-records two of them
         e.record(stream)
-    for _ in range(max(args.warmup, 3)):
-        step()
+    warm = max(args.warmup, 3)
+    for i in range(warm):
+        step(i)
     torch.cuda.synchronize()
     if int(dw.status.item()) != 0:
         raise RuntimeError(f"device status {int(dw.status.item())}")
 
+    # sustained load: the clock samples cover this window and the timed region
     clocks = ClockSampler(torch.cuda.current_device())
     barrier(world)
-    torch.cuda.synchronize()
     clocks.start()
-    time.sleep(0.3)
+    t_start = time.perf_counter()
+    i = warm
+    while time.perf_counter() - t_start < CLOCK_WINDOW_S:
+        for _ in range(32):
+            step(i)
+            i += 1
+        torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    launches0 = sk.splash_launch_count()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
-    for i in range(args.steps):
-        step(i)
+    for k in range(args.steps):
+        step(i + k, timed_k=k)
     t1.record(stream)
     torch.cuda.synchronize()
-    ck = clocks.stop()
+    launches = sk.splash_launch_count() - launches0
     barrier(world)
+    ck = clocks.stop()
     ms = t0.elapsed_time(t1) / args.steps
-    ms_max = reduce_max(ms, world)
-    attn_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(ev_a0, ev_a1))
+    ms_max = reduce_max(ms, world, dev)
+    if has_work:
+        attn_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(ev_b, ev_a))
+        t_attn_ms = statistics.mean(a.elapsed_time(c) for a, c in zip(ev_b, ev_c))
+    else:
+        attn_ms = t_attn_ms = 0.0
 
     # end to end through the public API with host buffers: H2D of the step's
     # inputs (q, k_new, v_new, lengths) from pinned memory, append + attention,
@@ -302,63 +389,79 @@ def run_ours(args):
     h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_ctx, h_T))
     d2h = sum(t.numel() * t.element_size() for t in (h_out, h_lse))
 
-    def e2e_step():
+    def e2e_step(j):
         dw.q.copy_(h_q, non_blocking=True)
         dw.k_new.copy_(h_k, non_blocking=True)
         dw.v_new.copy_(h_v, non_blocking=True)
         dw.ctx.copy_(h_ctx, non_blocking=True)
         dw.T.copy_(h_T, non_blocking=True)
-        dw.step()
+        dw.use_pool(j)
+        if has_work:
+            dw.step()
         h_out.copy_(dw.out, non_blocking=True)
         h_lse.copy_(dw.lse, non_blocking=True)
 
-    for _ in range(3):
-        e2e_step()
+    for j in range(3):
+        e2e_step(j)
     torch.cuda.synchronize()
     barrier(world)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
+    for j in range(args.steps):
+        e2e_step(j)
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = reduce_max(e0.elapsed_time(e1) / args.steps, world)
+    e2e_ms = reduce_max(e0.elapsed_time(e1) / args.steps, world, dev)
 
     peak, peak_src = load_peaks()
-    achieved = algo_bytes / (attn_ms * 1e-3) / 1e9
-    attn_kernel = "verify_tc" if args.path == 2 else "verify_attention"
+    achieved = algo_bytes / (t_attn_ms * 1e-3) / 1e9 if has_work else 0.0
+    kernel_only = algo_bytes / (attn_ms * 1e-3) / 1e9 if has_work else 0.0
+    n_tok = W_full.num_q_tokens
+    l2_note = (f"{n_copies} identical pool copies rotated step by step "
+               f"({n_copies} x {dw.pool_bytes() / 1e6:.0f} MB > 2 x L2)" if n_copies > 1 else
+               f"pool ({dw.pool_bytes() / 1e9:.2f} GB) larger than 2 x L2, no flush needed")
     line = {
         "metric": METRIC,
-        "value": world * n_tok / (ms_max * 1e-3),
+        "value": n_tok / (ms_max * 1e-3),
         "unit": UNIT,
         "n_gpus": world,
         "steps": args.steps,
-        "warmup": max(args.warmup, 3),
+        "warmup": warm,
         "ms_per_step": ms_max,
         "higher_is_better": True,
-        "scaling": "weak",
+        "scaling": "strong",
         "vs_baseline": None,
         "dtype": "int8 KV / bf16 Q,O / fp32 accumulate",
         "data": "synthetic (seeded; stands in for the pages' coding prompts)",
-        "config": {"workload": W.spec.name, "seqs": W.num_seqs, "context": int(W.context_lens.max()),
-                   "verify_block": int(W.block_lens.max()), "q_heads": spec.num_q_heads,
-                   "kv_heads": spec.num_kv_heads, "head_dim": spec.head_dim, "page": spec.page_size,
+        "config": {"workload": W_full.spec.name, "seqs": W_full.num_seqs,
+                   "context": int(W_full.context_lens.max()),
+                   "verify_block": int(W_full.block_lens.max()),
+                   "q_heads": W_full.spec.num_q_heads, "kv_heads": W_full.spec.num_kv_heads,
+                   "head_dim": W_full.spec.head_dim, "page": W_full.spec.page_size,
                    "verify_tokens_per_step": n_tok, "algorithmic_bytes": algo_bytes,
-                   "l2": "inputs larger than L2 (KV cache > 129 MB), no flush",
-                   "attention_ms": attn_ms, "hbm_gbs": achieved, "hbm_frac": achieved / peak,
-                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
+                   "l2": l2_note, "path": args.path,
+                   "t_attn_ms": t_attn_ms, "attention_kernel_ms": attn_ms,
+                   "hbm_gbs": achieved, "hbm_frac": achieved / peak,
+                   "parallelism": (f"{world} ranks, sequences partitioned by KV bytes"
+                                   if world > 1 else "1 GPU")},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "peak_source": f"{peak_src} (hbm_gbs, of {peak_src})",
-                     "kernel": attn_kernel,
-                     "traffic": kernel_traffic(attn_kernel, W.spec.name)},
-        "e2e": {"value": world * n_tok / (e2e_ms * 1e-3), "unit": UNIT,
+                     "frac": achieved / peak, "peak_source": f"hbm_gbs, of {peak_src}",
+                     "window": "verify_attention + lse_combine (events on the launching stream)",
+                     "attention_kernel_only": {"achieved": kernel_only,
+                                               "frac": kernel_only / peak},
+                     "kernel": "verify_attention",
+                     "traffic": kernel_traffic("verify_attention", W_full.spec.name)},
+        "e2e": {"value": n_tok / (e2e_ms * 1e-3), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": args.steps * dw_launches_per_step(W, args.path),
+        "gpu_launches": launches,
         "clocks": ck,
     }
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cb, _, _ = cpu_baseline(W, args.cpu_seconds)
+        one = cpu_baseline_one_core(args.workload, min(args.cpu_seconds, 8.0))
+        if one is not None:
+            cb["one_core"] = {"value": one["value"], "cores": one["cores"], "sample": one["sample"]}
         line["cpu_baseline"] = cb
     if rank == 0:
         print(json.dumps(line))
@@ -368,16 +471,14 @@ def run_ours(args):
     return 0
 
 
-def dw_launches_per_step(W: wl.Workload, path: int) -> int:
-    """Kernels one step launches: append, planner, attention kernel(s), combine."""
-    from speculative_verify_attention_kv_gb300 import splash_kv as sk
-    # one attention kernel: the tensor-core kernel takes every unit in automatic
-    # mode when it exists for the head size, else the CUDA-core kernel
-    return 1 + 1 + 1 + 1
-
-
 def main(argv=None):
     args = parse_args(argv)
+    if args.oracle_sample > 0:
+        cb, _, _ = cpu_baseline(wl.make(args.workload), args.oracle_sample)
+        print(json.dumps(cb))
+        return 0
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        return relaunch_under_torchrun(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

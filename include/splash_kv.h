@@ -94,6 +94,11 @@ int splash_abi_version(void);
  * (units then run on the CUDA-core kernel). */
 int splash_tensor_path_supported(int head_dim);
 
+/* Number of kernels the library has enqueued since it was loaded (all entry
+ * points, all threads; a host-side count of successful launches). Lets a
+ * caller count the device work one call or one benchmark step issues. */
+unsigned long long splash_launch_count(void);
+
 /* Limit, in nanoseconds, of every internal pipeline wait of the tensor-core
  * attention kernel for the launches that follow (process-wide; 0 restores the
  * default of 1 s). When a wait runs out, the kernel stops the call's work,

@@ -51,6 +51,12 @@ bool head_dim_ok(int d) { return d == 64 || d == 128 || d == 256; }
 
 constexpr unsigned long long kDefaultWaitNs = 1000000000ull;   // 1 s
 std::atomic<unsigned long long> g_wait_limit_ns{kDefaultWaitNs};
+std::atomic<unsigned long long> g_launches{0};               // kernels enqueued so far
+
+cudaError_t counted(cudaError_t e) {
+  if (e == cudaSuccess) g_launches.fetch_add(1, std::memory_order_relaxed);
+  return e;
+}
 
 // CTAs per class: the tensor-core kernel runs one CTA per SM, the CUDA-core
 // kernel as many as fit.
@@ -90,6 +96,8 @@ const char* splash_status_string(int status) {
 // 2: one interleaved K/V code pool (v_pages = k_pages + P * D)
 int splash_abi_version(void) { return 2; }
 
+unsigned long long splash_launch_count(void) { return g_launches.load(); }
+
 unsigned long long splash_set_wait_limit_ns(unsigned long long ns) {
   return g_wait_limit_ns.exchange(ns == 0 ? kDefaultWaitNs : ns);
 }
@@ -113,10 +121,10 @@ int splash_kv_append(const float* k_new, const float* v_new, int num_new_tokens,
   if (!k_new || !v_new || !k_pages || !v_pages || !k_scales || !v_scales || !page_table ||
       !context_lens || !block_lens)
     return SPLASH_ERR_INVALID_ARGUMENT;
-  cudaError_t e = launch_kv_append(k_new, v_new, num_new_tokens, k_pages, v_pages, k_scales,
-                                   v_scales, page_table, max_pages_per_seq, context_lens,
-                                   block_lens, num_seqs, num_kv_heads, head_dim, num_pages,
-                                   device_status, stream);
+  cudaError_t e = counted(launch_kv_append(k_new, v_new, num_new_tokens, k_pages, v_pages,
+                                           k_scales, v_scales, page_table, max_pages_per_seq,
+                                           context_lens, block_lens, num_seqs, num_kv_heads,
+                                           head_dim, num_pages, device_status, stream));
   return e == cudaSuccess ? SPLASH_OK : SPLASH_ERR_CUDA;
 }
 
@@ -136,11 +144,11 @@ int splash_kv_append_bf16(const uint16_t* k_new, const uint16_t* v_new, int num_
   if (!k_new || !v_new || !k_pages || !v_pages || !k_scales || !v_scales || !page_table ||
       !context_lens || !block_lens)
     return SPLASH_ERR_INVALID_ARGUMENT;
-  cudaError_t e = launch_kv_append_bf16(
+  cudaError_t e = counted(launch_kv_append_bf16(
       reinterpret_cast<const __nv_bfloat16*>(k_new), reinterpret_cast<const __nv_bfloat16*>(v_new),
       num_new_tokens, k_pages, v_pages, k_scales, v_scales, page_table, max_pages_per_seq,
       context_lens, block_lens, num_seqs, num_kv_heads, head_dim, num_pages, device_status,
-      stream);
+      stream));
   return e == cudaSuccess ? SPLASH_OK : SPLASH_ERR_CUDA;
 }
 
@@ -153,9 +161,10 @@ int splash_accept_commit(const int32_t* block_tokens, const int32_t* target_toke
   if (!block_lens || !context_lens || !accepted || !next_tokens ||
       (num_tokens > 0 && (!block_tokens || !target_tokens)))
     return SPLASH_ERR_INVALID_ARGUMENT;
-  cudaError_t e = launch_accept_commit(block_tokens, target_tokens, num_tokens, block_lens,
-                                       context_lens, accepted, next_tokens, num_seqs,
-                                       device_status, reinterpret_cast<cudaStream_t>(stream));
+  cudaError_t e = counted(launch_accept_commit(block_tokens, target_tokens, num_tokens,
+                                               block_lens, context_lens, accepted, next_tokens,
+                                               num_seqs, device_status,
+                                               reinterpret_cast<cudaStream_t>(stream)));
   return e == cudaSuccess ? SPLASH_OK : SPLASH_ERR_CUDA;
 }
 
@@ -253,10 +262,10 @@ static int verify_impl(
   // go to the tensor-core kernel (the planner's row threshold already does so
   // for every unit with >= 16 rows).
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_plan(context_lens, block_lens, num_seqs, num_kv_heads, G,
+  cudaError_t e = counted(launch_plan(context_lens, block_lens, num_seqs, num_kv_heads, G,
                               max_pages_per_seq, max_block_len, use_tt ? tt_tile_keys() : kTcTile,
                               kSimtTile, nt, ns, path,
-                              (int)rb, num_q_tokens, window, ws, device_status, s);
+                              (int)rb, num_q_tokens, window, ws, device_status, s));
   if (e != cudaSuccess) return SPLASH_ERR_CUDA;
 
   AttnParams p;
@@ -283,17 +292,17 @@ static int verify_impl(
   if (attn_begin && cudaEventRecord(reinterpret_cast<cudaEvent_t>(attn_begin), s) != cudaSuccess)
     return SPLASH_ERR_CUDA;
   if (path != 1 && tc_ok) {
-    e = use_tt ? launch_verify_tt(p, tmap, nt, s) : launch_verify_tc(p, rows_cap, nt, s);
+    e = counted(use_tt ? launch_verify_tt(p, tmap, nt, s) : launch_verify_tc(p, rows_cap, nt, s));
     if (e != cudaSuccess) return SPLASH_ERR_CUDA;
   }
   if (path != 2 && rows_simt > 0) {
-    e = launch_verify_simt(p, rows_simt, ns, s);
+    e = counted(launch_verify_simt(p, rows_simt, ns, s));
     if (e != cudaSuccess) return SPLASH_ERR_CUDA;
   }
   if (attn_end && cudaEventRecord(reinterpret_cast<cudaEvent_t>(attn_end), s) != cudaSuccess)
     return SPLASH_ERR_CUDA;
-  e = launch_combine(num_q_tokens, num_q_heads, num_seqs, num_kv_heads, G, head_dim, (int)rb, ws,
-                     p.out, lse, s);
+  e = counted(launch_combine(num_q_tokens, num_q_heads, num_seqs, num_kv_heads, G, head_dim,
+                             (int)rb, ws, p.out, lse, s));
   return e == cudaSuccess ? SPLASH_OK : SPLASH_ERR_CUDA;
 }
 

@@ -80,6 +80,23 @@ class DeviceWorkload:
         if int(self.status.item()) != 0:
             raise RuntimeError(f"device status {int(self.status.item())} while populating")
 
+    # ---- pool copies (to run steps on inputs that L2 cannot hold) --------
+    def pool_bytes(self) -> int:
+        return sum(t.numel() * t.element_size() for t in (self.pool[0]._base, self.pool[2], self.pool[3]))
+
+    def add_pool_copies(self, n: int):
+        """n identical pools in total; use_pool(i) selects copy i % n."""
+        base = self.pool[0]._base
+        self.pools = [self.pool]
+        for _ in range(n - 1):
+            codes = base.clone()
+            self.pools.append((codes[:, :, 0], codes[:, :, 1], self.pool[2].clone(),
+                               self.pool[3].clone()))
+
+    def use_pool(self, i: int):
+        pools = getattr(self, "pools", [self.pool])
+        self.pool = pools[i % len(pools)]
+
     # ---- one step: append the verify block, attend ----------------------
     def append_block(self, stream=None):
         sk.splash_kv_append(self.k_new, self.v_new, *self.pool, self.table, self.ctx, self.T,

@@ -44,6 +44,8 @@ def _load() -> ctypes.CDLL:
     lib.splash_abi_version.restype = I
     lib.splash_tensor_path_supported.restype = I
     lib.splash_tensor_path_supported.argtypes = [I]
+    lib.splash_launch_count.restype = ctypes.c_ulonglong
+    lib.splash_launch_count.argtypes = []
     lib.splash_set_wait_limit_ns.restype = ctypes.c_ulonglong
     lib.splash_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
     lib.splash_kv_append.restype = I
@@ -72,7 +74,7 @@ def _load() -> ctypes.CDLL:
 
 LIB = _load()
 EXPORTED = ("splash_status_string", "splash_abi_version", "splash_tensor_path_supported",
-            "splash_set_wait_limit_ns",
+            "splash_set_wait_limit_ns", "splash_launch_count",
             "splash_kv_append", "splash_kv_append_bf16", "splash_accept_commit",
             "splash_verify_attention_swa",
             "splash_verify_attention_workspace_size", "splash_verify_attention",
@@ -82,6 +84,11 @@ EXPORTED = ("splash_status_string", "splash_abi_version", "splash_tensor_path_su
 
 def tensor_path_available(head_dim: int) -> bool:
     return bool(LIB.splash_tensor_path_supported(int(head_dim)))
+
+
+def splash_launch_count() -> int:
+    """Kernels the library has enqueued since it was loaded."""
+    return int(LIB.splash_launch_count())
 
 
 def splash_set_wait_limit_ns(ns: int) -> int:

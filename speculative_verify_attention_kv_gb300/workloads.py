@@ -164,6 +164,20 @@ class Workload:
         self.q_offsets = np.concatenate([[0], np.cumsum(T)]).astype(np.int64)
         self.num_q_tokens = int(T.sum())
         self.sm_scale = np.float32(1.0 / math.sqrt(s.head_dim))
+        # key of each sequence's random streams ([seed, 1, b, h] ...): its own
+        # index, or its index in the parent workload for a subset
+        self.seq_ids = np.arange(self.num_seqs)
+
+    def subset(self, seqs) -> "Workload":
+        """The listed sequences as a workload of their own: the same lengths,
+        outlier channels and data (every sequence keeps its random streams) on
+        a compact page pool (a shared prefix stays shared)."""
+        seqs = np.asarray(seqs, dtype=np.int64)
+        sub = Workload(self.spec, self.seed, context_lens=self.context_lens[seqs],
+                       block_lens=self.block_lens[seqs], shared_prefix_len=self.prefix_len)
+        sub.outlier_channels = self.outlier_channels
+        sub.seq_ids = self.seq_ids[seqs]
+        return sub
 
     # ---- tensors --------------------------------------------------------
     def _apply_outliers(self, x: np.ndarray, h: int) -> np.ndarray:
@@ -183,8 +197,9 @@ class Workload:
         fp32 [context_len - prefix_len, D] each."""
         D = self.spec.head_dim
         n = int(self.context_lens[b]) - self.prefix_len
-        k = _normal([self.seed, 1, b, h], (n, D))
-        v = _normal([self.seed, 2, b, h], (n, D))
+        sid = int(self.seq_ids[b])
+        k = _normal([self.seed, 1, sid, h], (n, D))
+        v = _normal([self.seed, 2, sid, h], (n, D))
         return self._apply_outliers(k, h), self._apply_outliers(v, h)
 
     def context_kv(self, b: int, h: int):
@@ -201,7 +216,7 @@ class Workload:
         T = int(self.block_lens[b])
         ks, vs = [], []
         for h in range(s.num_kv_heads):
-            rng = np.random.default_rng([self.seed, 3, b, h])
+            rng = np.random.default_rng([self.seed, 3, int(self.seq_ids[b]), h])
             k = rng.standard_normal((T, s.head_dim), dtype=np.float32)
             v = rng.standard_normal((T, s.head_dim), dtype=np.float32)
             ks.append(self._apply_outliers(k, h))
@@ -221,7 +236,7 @@ class Workload:
     def q_bits_seq(self, b: int) -> np.ndarray:
         s = self.spec
         T = int(self.block_lens[b])
-        q = _normal([self.seed, 4, b], (T, s.num_q_heads, s.head_dim))
+        q = _normal([self.seed, 4, int(self.seq_ids[b])], (T, s.num_q_heads, s.head_dim))
         return bf16_bits_from_f32(q)
 
     def q_bits(self) -> np.ndarray:
@@ -251,6 +266,22 @@ class Workload:
         kv = slots * s.num_kv_heads * (2 * s.head_dim + 8)
         qo = 2 * self.num_q_tokens * s.num_q_heads * s.head_dim * 2
         return kv + qo
+
+
+def partition_by_kv_bytes(W: Workload, parts: int):
+    """Split W's sequences into `parts` groups of nearly equal KV bytes (the
+    work of a sequence is proportional to its ctx + T keys): largest first,
+    each to the group with the least so far (lowest index on ties). Returns
+    sorted sequence lists, one per group."""
+    cost = W.context_lens.astype(np.int64) + W.block_lens
+    order = sorted(range(W.num_seqs), key=lambda b: (-int(cost[b]), b))
+    load = [0] * parts
+    groups = [[] for _ in range(parts)]
+    for b in order:
+        r = min(range(parts), key=lambda i: (load[i], i))
+        groups[r].append(b)
+        load[r] += int(cost[b])
+    return [sorted(g) for g in groups]
 
 
 def make(name_or_index, seed: int | None = None) -> Workload:
