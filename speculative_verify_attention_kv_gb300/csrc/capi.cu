@@ -64,8 +64,8 @@ void default_ctas(int sms, int head_dim, int rows_cap, int* ncta_tc, int* ncta_s
   const size_t smem = simt_smem_bytes(head_dim, rows_cap);
   int per_sm = smem ? (int)((227 * 1024) / (smem + 1024)) : 1;
   per_sm = per_sm < 1 ? 1 : (per_sm > 4 ? 4 : per_sm);
-  *ncta_tc = sms;
-  *ncta_simt = sms * per_sm;
+  *ncta_tc = sms < kMaxCtas ? sms : kMaxCtas;
+  *ncta_simt = sms * per_sm < kMaxCtas ? sms * per_sm : kMaxCtas;
 }
 
 long long rows_bound_for(int num_q_tokens, int num_q_heads, int rows_cap, int ncta_tc,
@@ -214,7 +214,8 @@ static int verify_impl(
   int st = check_attn_shape(num_q_tokens, num_seqs, num_q_heads, num_kv_heads, head_dim,
                             page_size, max_block_len, max_pages_per_seq);
   if (st != SPLASH_OK) return st;
-  if (path < 0 || path > 3 || ctas_per_class < 0 || num_pages < 0 || window < 0)
+  if (path < 0 || path > 3 || ctas_per_class < 0 || ctas_per_class > kMaxCtas || num_pages < 0 ||
+      window < 0)
     return SPLASH_ERR_INVALID_ARGUMENT;
   if (num_q_tokens == 0 || num_seqs == 0) return SPLASH_OK;
   if (k_pages && v_pages && v_pages != k_pages + (size_t)page_size * head_dim)

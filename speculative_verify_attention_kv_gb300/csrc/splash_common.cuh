@@ -22,6 +22,17 @@ constexpr int kMaxRows = 128;     // T*G limit per sequence and KV head
 // there when a tensor-core kernel exists for the head size.
 constexpr int kTensorMinRows = 1;
 
+// Split of a class's tile stream over its CTAs by estimated cost, not by tile
+// count (a CTA's range is [cta_start[c], cta_start[c+1])). Cost of one tile of
+// a unit with R query rows: tile_cost + R * row_cost; every unit adds
+// segment_cost for the pipeline fill / drain of a segment. Measured on the
+// tensor-core kernel (64-key tiles, ragged T in {1, 4, 8, 16}, G = 6): a tile
+// costs 1.22 us at R = 6 and 1.37 us at R = 96, a segment start ~7.5 us.
+constexpr int kMaxCtas = 1023;                 // per class (starts fit one 1024-thread scan)
+__host__ __device__ constexpr long long tile_cost(int cls) { return cls == kClassTensor ? 4096 : 1024; }
+__host__ __device__ constexpr long long row_cost(int cls) { return cls == kClassTensor ? 6 : 256; }
+__host__ __device__ constexpr long long segment_cost(int cls) { return cls == kClassTensor ? 6 * 4096 : 4096; }
+
 // Plan written by the planner kernel at the start of the workspace.
 struct PlanHeader {
   int total_tiles[kNumClasses];   // key tiles of all (seq, KV head) units of a class
@@ -71,6 +82,8 @@ struct WorkspaceLayout {
   size_t nseg;         // int32 [B*Hkv] CTAs (segments) that cover the unit
   size_t cfirst;       // int32 [B*Hkv] first CTA of the unit
   size_t part_base;    // int32 [B*Hkv] first partial row of the unit
+  size_t wcost;        // int64 [2][B+1] per-class exclusive prefix of sequence costs
+  size_t cta_start;    // int32 [2][kMaxCtas+1] first tile of each CTA, per class
   size_t o_part;       // fp32  [rows_bound, D]
   size_t lse_part;     // fp32  [rows_bound]
   size_t total;
@@ -89,21 +102,14 @@ __host__ __device__ inline WorkspaceLayout make_layout(int B, int Hkv, int D, lo
   L.nseg = o;       o = align256(o + sizeof(int) * (size_t)B * Hkv);
   L.cfirst = o;     o = align256(o + sizeof(int) * (size_t)B * Hkv);
   L.part_base = o;  o = align256(o + sizeof(int) * (size_t)B * Hkv);
+  L.wcost = o;      o = align256(o + sizeof(long long) * (size_t)kNumClasses * (B + 1));
+  L.cta_start = o;  o = align256(o + sizeof(int) * (size_t)kNumClasses * (kMaxCtas + 1));
   L.o_part = o;     o = align256(o + sizeof(float) * (size_t)rows_bound * D);
   L.lse_part = o;   o = align256(o + sizeof(float) * (size_t)rows_bound);
   L.total = o;
   return L;
 }
 
-// Split of a class's tile stream over its persistent CTAs: CTA c owns tiles
-// [tile_begin(c), tile_begin(c+1)).
-__host__ __device__ inline int tile_begin(int c, int total, int ncta) {
-  return (int)(((long long)c * total) / ncta);
-}
-// The CTA whose range contains tile t (0 <= t < total).
-__host__ __device__ inline int cta_of_tile(int t, int total, int ncta) {
-  return (int)((((long long)t + 1) * ncta - 1) / total);
-}
 
 struct AttnParams {
   const __nv_bfloat16* q;
@@ -128,6 +134,33 @@ struct AttnParams {
   int* device_status;
 };
 
+// Programmatic dependent launch: a kernel launched with launch_dependent()
+// may start while the kernel before it on the stream is still running; it
+// calls grid_dependency_wait() before it reads anything that kernel wrote
+// (a no-op for a kernel launched the ordinary way). allow_dependent_launch()
+// lets the next such kernel be scheduled early.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void allow_dependent_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                    cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 __device__ inline void report(int* status, int code) {
   if (status) atomicCAS(status, 0, code);
 }
@@ -144,7 +177,8 @@ __device__ inline float warp_sum(float v) {
 }
 
 // Largest index i in [0, n] with a[i] <= x, for a non-decreasing array a[0..n].
-__device__ inline int upper_index(const int* a, int n, int x) {
+template <typename V>
+__device__ inline int upper_index(const V* a, int n, V x) {
   int lo = 0, hi = n;
   while (lo < hi) {
     int mid = (lo + hi + 1) >> 1;

@@ -4,7 +4,8 @@
 // 0 .. ctx_b + T_b - 1 (with a sliding window W, from the tile holding key
 // ctx_b - W + 1 on). Each unit is cut into key tiles; the tiles of all units
 // of one class (tensor-core or CUDA-core kernel) form one stream that is split
-// evenly over that kernel's persistent CTAs. A unit touched by one CTA is
+// over that kernel's persistent CTAs into ranges of about equal estimated cost
+// (per-tile cost grows with the unit's rows; each unit start adds a fill cost). A unit touched by one CTA is
 // finished by it; a unit touched by n > 1 CTAs leaves n partials (o_i
 // normalised by its own sum, lse_i) that lse_combine merges:
 //   lse = ln sum_i exp(lse_i),  O = sum_i exp(lse_i - lse) o_i
@@ -14,6 +15,32 @@
 namespace splash {
 
 constexpr int kPlanThreads = 1024;
+
+// Inclusive max-scan over the CTA (kPlanThreads threads).
+__device__ inline int block_inclusive_max(int v, int* s_warp) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl = max(incl, y);
+  }
+  if (lane == 31) s_warp[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int x = s_warp[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x = max(x, y);
+    }
+    s_warp[lane] = x;
+  }
+  __syncthreads();
+  const int res = warp ? max(s_warp[warp - 1], incl) : incl;
+  __syncthreads();
+  return res;
+}
 
 // Exclusive scan over the CTA (kPlanThreads threads); *total receives the sum.
 template <typename V>
@@ -50,6 +77,8 @@ plan_kernel(const int32_t* __restrict__ context_lens, const int32_t* __restrict_
             int num_q_tokens, int window, unsigned char* ws, int* device_status) {
   __shared__ int s_warp[32];
   __shared__ long long s_warp64[32];
+  __shared__ int s_start[kNumClasses][kMaxCtas + 1];
+  allow_dependent_launch();        // the attention kernel may get its SMs now
   const WorkspaceLayout L = make_layout(num_seqs, num_kv_heads, 0, rows_bound);
   int* q_off = reinterpret_cast<int*>(ws + L.q_off);
   int* seq_T = reinterpret_cast<int*>(ws + L.seq_T);
@@ -59,6 +88,8 @@ plan_kernel(const int32_t* __restrict__ context_lens, const int32_t* __restrict_
   int* nseg = reinterpret_cast<int*>(ws + L.nseg);
   int* cfirst = reinterpret_cast<int*>(ws + L.cfirst);
   int* part_base = reinterpret_cast<int*>(ws + L.part_base);
+  long long* wcost = reinterpret_cast<long long*>(ws + L.wcost);
+  int* cta_start = reinterpret_cast<int*>(ws + L.cta_start);
   const int tile[kNumClasses] = {tile_tc, tile_simt};
   const int ncta[kNumClasses] = {ncta_tc, ncta_simt};
 
@@ -66,7 +97,7 @@ plan_kernel(const int32_t* __restrict__ context_lens, const int32_t* __restrict_
   // The Q / O rows of sequence b start at the sum of the caller's block_lens
   // before it (negative lengths count as 0), whether or not b itself is valid:
   // a rejected sequence is idle, and the others keep their rows.
-  long long run_q = 0;
+  long long run_q = 0, run_w[kNumClasses] = {0, 0};
   int run_t0 = 0, run_t1 = 0;
   for (int base = 0; base < num_seqs; base += kPlanThreads) {
     const int b = base + threadIdx.x;
@@ -105,11 +136,24 @@ plan_kernel(const int32_t* __restrict__ context_lens, const int32_t* __restrict_
     const int t1 = block_exclusive_scan(cls == 1 ? tiles * num_kv_heads : 0, s_warp, &tot);
     if (b < num_seqs) stp[(num_seqs + 1) + b] = run_t1 + t1;
     run_t1 += tot;
+    // estimated cost of the sequence's units, per class (see tile_cost)
+#pragma unroll
+    for (int c = 0; c < kNumClasses; ++c) {
+      const long long cost =
+          cls == c ? (long long)num_kv_heads *
+                         ((long long)tiles * (tile_cost(c) + row_cost(c) * T * group) + segment_cost(c))
+                   : 0;
+      long long totw;
+      const long long w0 = block_exclusive_scan(cost, s_warp64, &totw);
+      if (b < num_seqs) wcost[c * (num_seqs + 1) + b] = run_w[c] + w0;
+      run_w[c] += totw;
+    }
   }
   if (threadIdx.x == 0) {
     q_off[num_seqs] = (int)min(run_q, (long long)num_q_tokens);
     stp[num_seqs] = run_t0;
     stp[(num_seqs + 1) + num_seqs] = run_t1;
+    for (int c = 0; c < kNumClasses; ++c) wcost[c * (num_seqs + 1) + num_seqs] = run_w[c];
   }
   __syncthreads();
   // block lengths that sum past the q / out rows the caller passed: do nothing
@@ -124,7 +168,48 @@ plan_kernel(const int32_t* __restrict__ context_lens, const int32_t* __restrict_
   // a class's kernel uses at most one CTA per tile, so that every CTA it uses
   // owns >= 1 tile and the CTAs covering a unit are consecutive, all non-empty
   int ncta_eff[kNumClasses];
-  for (int c = 0; c < kNumClasses; ++c) ncta_eff[c] = min(ncta[c], total[c]);
+  for (int c = 0; c < kNumClasses; ++c) ncta_eff[c] = min(min(ncta[c], total[c]), kMaxCtas);
+
+  // CTA c of a class starts where the class's cumulative cost reaches
+  // c / n of its total: find the sequence, then the unit (KV head), then the
+  // tile (the first segment_cost of a unit maps to its first tile). Then the
+  // starts are made strictly increasing (every CTA owns >= 1 tile) and the
+  // last ones are pulled back so that CTA n - 1 still fits before `total`.
+  for (int c = 0; c < kNumClasses; ++c) {
+    const int n = ncta_eff[c];
+    const long long* wc = wcost + c * (num_seqs + 1);
+    const int* sp = stp + c * (num_seqs + 1);
+    static_assert(kMaxCtas + 1 <= kPlanThreads, "one start per planner thread");
+    {
+      const int k = threadIdx.x;
+      int start = 0;
+      if (k <= n && n > 0 && rows_ok) {
+        if (k == n) {
+          start = total[c];
+        } else if (k > 0) {
+          const long long target = run_w[c] * k / n;      // < 2^63 for any realistic batch
+          const int b = upper_index(wc, num_seqs - 1, target);
+          const long long off = target - wc[b];
+          const int T = seq_T[b];
+          const int tiles = unit_tiles(seq_ctx[b], T, window, tile[c]);
+          const long long w = tile_cost(c) + row_cost(c) * T * group;
+          const long long uc = (long long)tiles * w + segment_cost(c);
+          const int h = (int)min(off / uc, (long long)num_kv_heads - 1);
+          const long long rem = off - h * uc;
+          const int t = rem < segment_cost(c) ? 0 : (int)min((rem - segment_cost(c)) / w, (long long)tiles - 1);
+          start = sp[b] + h * tiles + t;
+        }
+      }
+      // strictly increasing: prefix max of start - k, plus k
+      const int y = block_inclusive_max(k <= n ? start - k : -(1 << 30), s_warp);
+      if (k <= n) s_start[c][k] = min(y + k, total[c] - (n - k));
+      __syncthreads();
+    }
+  }
+  __syncthreads();
+  for (int c = 0; c < kNumClasses; ++c)
+    for (int k = threadIdx.x; k <= ncta_eff[c]; k += kPlanThreads)
+      cta_start[c * (kMaxCtas + 1) + k] = s_start[c][k];
 
   // pass 2: per unit (b, h) — segments and partial rows
   const int num_units = num_seqs * num_kv_heads;
@@ -139,12 +224,12 @@ plan_kernel(const int32_t* __restrict__ context_lens, const int32_t* __restrict_
       if (cls >= 0) {
         const int T = seq_T[b], ctx = seq_ctx[b];
         const int tk = cls == 0 ? tile[0] : tile[1];        // selects, not a local-memory index
-        const int tot = cls == 0 ? total[0] : total[1];
         const int nce = cls == 0 ? ncta_eff[0] : ncta_eff[1];
         const int tiles = unit_tiles(ctx, T, window, tk);
         const int tp = stp[cls * (num_seqs + 1) + b] + h * tiles;
-        cf = cta_of_tile(tp, tot, nce);
-        const int cl = cta_of_tile(tp + tiles - 1, tot, nce);
+        const int* cs = s_start[cls == 0 ? 0 : 1];
+        cf = upper_index(cs, nce - 1, tp);
+        const int cl = upper_index(cs, nce - 1, tp + tiles - 1);
         ns = cl - cf + 1;
         if (ns > 1) rows = ns * T * group;
       }
@@ -180,6 +265,7 @@ lse_combine_kernel(int num_q_tokens, int num_q_heads, int num_seqs, int num_kv_h
                    int rows_bound, const unsigned char* __restrict__ ws,
                    __nv_bfloat16* __restrict__ out, float* __restrict__ lse_out) {
   constexpr int EPL = D / 32;
+  grid_dependency_wait();          // the attention kernel's partials are complete
   const WorkspaceLayout L = make_layout(num_seqs, num_kv_heads, D, rows_bound);
   const int* q_off = reinterpret_cast<const int*>(ws + L.q_off);
   const int* seq_T = reinterpret_cast<const int*>(ws + L.seq_T);
@@ -267,8 +353,9 @@ cudaError_t launch_combine(int num_q_tokens, int num_q_heads, int num_seqs, int 
   if (rows == 0) return cudaSuccess;
   const int grid = (int)((rows + 7) / 8);
 #define SPLASH_COMBINE(DD)                                                                     \
-  lse_combine_kernel<DD><<<grid, 256, 0, stream>>>(num_q_tokens, num_q_heads, num_seqs,       \
-                                                   num_kv_heads, group, rows_bound, ws, out, lse)
+  e = launch_dependent(lse_combine_kernel<DD>, dim3(grid), dim3(256), 0, stream, num_q_tokens, \
+                       num_q_heads, num_seqs, num_kv_heads, group, rows_bound, ws, out, lse)
+  cudaError_t e = cudaSuccess;
   switch (head_dim) {
     case 64: SPLASH_COMBINE(64); break;
     case 128: SPLASH_COMBINE(128); break;
@@ -276,7 +363,7 @@ cudaError_t launch_combine(int num_q_tokens, int num_q_heads, int num_seqs, int 
     default: return cudaErrorInvalidValue;
   }
 #undef SPLASH_COMBINE
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace splash

@@ -44,6 +44,8 @@ verify_simt_kernel(AttnParams p, int rows_cap) {
   float* l_s = m_s + rows_cap;
   float* a_s = l_s + rows_cap;
 
+  grid_dependency_wait();          // the split plan is complete
+  allow_dependent_launch();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int B = p.num_seqs, Hkv = p.num_kv_heads, G = p.group;
   const WorkspaceLayout L = make_layout(B, Hkv, D, reinterpret_cast<const PlanHeader*>(p.ws)->rows_bound);
@@ -62,8 +64,9 @@ verify_simt_kernel(AttnParams p, int rows_cap) {
   const int ncta = hd->ncta[kClassSimt];
   const int window = hd->window;
   if ((int)blockIdx.x >= ncta) return;
-  int t = tile_begin(blockIdx.x, total, ncta);
-  const int t_end = tile_begin(blockIdx.x + 1, total, ncta);
+  const int* cst = reinterpret_cast<const int*>(p.ws + L.cta_start) + kClassSimt * (kMaxCtas + 1);
+  int t = cst[blockIdx.x];
+  const int t_end = cst[blockIdx.x + 1];
 
   while (t < t_end) {
     const int b = upper_index(stp, B - 1, t);
@@ -243,7 +246,9 @@ cudaError_t launch_verify_simt(const AttnParams& p, int rows_cap, int ncta, cuda
     cudaError_t e = cudaFuncSetAttribute(verify_simt_kernel<DD>,                               \
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); \
     if (e != cudaSuccess) return e;                                                            \
-    verify_simt_kernel<DD><<<ncta, kSimtThreads, smem, stream>>>(p, rows_cap);                 \
+    e = launch_dependent(verify_simt_kernel<DD>, dim3(ncta), dim3(kSimtThreads), smem, stream, \
+                         p, rows_cap);                                                         \
+    if (e != cudaSuccess) return e;                                                            \
   } while (0)
   switch (p.head_dim) {
     case 64: SPLASH_SIMT(64); break;

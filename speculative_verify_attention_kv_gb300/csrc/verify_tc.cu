@@ -500,6 +500,8 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
   using C = Cfg<D>;
   static_assert(sizeof(Smem) <= C::kBarBytes, "barrier area");
   extern __shared__ uint8_t smem_raw[];
+  grid_dependency_wait();          // the split plan is complete
+  allow_dependent_launch();
   const PlanHeader* hd = reinterpret_cast<const PlanHeader*>(p.ws);
   const int total = hd->total_tiles[kClassTensor];
   const int ncta = hd->ncta[kClassTensor];
@@ -568,8 +570,8 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
   const Sync sync{&sh->abort_flag, p.device_status, p.wait_ns};
 
   const int window = kSwa ? p.window : 0;
-  SegIter iter{stp, seq_T, seq_ctx, B, G, Hkv, window, tile_begin(blockIdx.x, total, ncta),
-               tile_begin(blockIdx.x + 1, total, ncta)};
+  const int* cst = reinterpret_cast<const int*>(p.ws + L.cta_start) + kClassTensor * (kMaxCtas + 1);
+  SegIter iter{stp, seq_T, seq_ctx, B, G, Hkv, window, cst[blockIdx.x], cst[blockIdx.x + 1]};
 
   if (warp < kSoftmaxWarps) {
     // ===================================================== softmax + epilogue
@@ -1022,7 +1024,9 @@ cudaError_t launch_verify_tc(const AttnParams& p, int rows_cap, int ncta, cudaSt
     cudaError_t e = cudaFuncSetAttribute(tc::verify_tc_kernel<DD, SWA>,                        \
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);   \
     if (e != cudaSuccess) return e;                                                            \
-    tc::verify_tc_kernel<DD, SWA><<<ncta, tc::kThreads, smem, stream>>>(p);                   \
+    e = launch_dependent(tc::verify_tc_kernel<DD, SWA>, dim3(ncta), dim3(tc::kThreads), smem,  \
+                         stream, p);                                                           \
+    if (e != cudaSuccess) return e;                                                            \
   } while (0)
   const bool swa = p.window > 0;
   switch (p.head_dim) {

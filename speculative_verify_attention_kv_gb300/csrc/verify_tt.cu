@@ -256,6 +256,8 @@ template <bool kSwa>
 __global__ void __launch_bounds__(kThreads, 1)
 verify_tt_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmap) {
   extern __shared__ uint8_t smem_raw[];
+  grid_dependency_wait();          // the split plan is complete
+  allow_dependent_launch();
   const PlanHeader* hd = reinterpret_cast<const PlanHeader*>(p.ws);
   const int total = hd->total_tiles[kClassTensor];
   const int ncta = hd->ncta[kClassTensor];
@@ -331,8 +333,8 @@ verify_tt_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmap) {
   const uint32_t tmem = sh->tmem_base;
   const Sync sync{&sh->abort_flag, p.device_status, p.wait_ns};
   const int window = kSwa ? p.window : 0;
-  SegIter iter{stp, seq_T, seq_ctx, B, G, Hkv, window, tile_begin(blockIdx.x, total, ncta),
-               tile_begin(blockIdx.x + 1, total, ncta)};
+  const int* cst = reinterpret_cast<const int*>(p.ws + L.cta_start) + kClassTensor * (kMaxCtas + 1);
+  SegIter iter{stp, seq_T, seq_ctx, B, G, Hkv, window, cst[blockIdx.x], cst[blockIdx.x + 1]};
 
   // Register split: the softmax warpgroups (warps 0-7) take 160 registers a
   // thread, the converter / MMA warpgroups 96: 256 x 160 + 256 x 96 = 65536,
@@ -979,12 +981,16 @@ cudaError_t launch_verify_tt(const AttnParams& p, const CUtensorMap& map, int nc
     e = cudaFuncSetAttribute(tt::verify_tt_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              smem);
     if (e != cudaSuccess) return e;
-    tt::verify_tt_kernel<true><<<ncta, tt::kThreads, smem, stream>>>(p, map);
+    e = launch_dependent(tt::verify_tt_kernel<true>, dim3(ncta), dim3(tt::kThreads), smem, stream, p,
+                         map);
+    if (e != cudaSuccess) return e;
   } else {
     e = cudaFuncSetAttribute(tt::verify_tt_kernel<false>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    tt::verify_tt_kernel<false><<<ncta, tt::kThreads, smem, stream>>>(p, map);
+    e = launch_dependent(tt::verify_tt_kernel<false>, dim3(ncta), dim3(tt::kThreads), smem, stream, p,
+                         map);
+    if (e != cudaSuccess) return e;
   }
   return cudaGetLastError();
 }
