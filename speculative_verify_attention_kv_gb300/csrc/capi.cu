@@ -18,7 +18,7 @@ cudaError_t launch_accept_commit(const int32_t*, const int32_t*, int, const int3
                                  int32_t*, int32_t*, int, int*, cudaStream_t);
 cudaError_t launch_plan(const int32_t*, const int32_t*, int, int, int, int, int, int, int, int,
                         int, int, int, int, int, unsigned char*, int*, cudaStream_t);
-cudaError_t launch_combine(int, int, int, int, int, int, int, const unsigned char*,
+cudaError_t launch_combine(int, int, int, int, int, int, int, int, const unsigned char*,
                            __nv_bfloat16*, float*, cudaStream_t);
 cudaError_t launch_verify_simt(const AttnParams&, int, int, cudaStream_t);
 size_t simt_smem_bytes(int, int);
@@ -303,7 +303,7 @@ static int verify_impl(
   if (attn_end && cudaEventRecord(reinterpret_cast<cudaEvent_t>(attn_end), s) != cudaSuccess)
     return SPLASH_ERR_CUDA;
   e = counted(launch_combine(num_q_tokens, num_q_heads, num_seqs, num_kv_heads, G, head_dim,
-                             (int)rb, ws, p.out, lse, s));
+                             (int)rb, sms, ws, p.out, lse, s));
   return e == cudaSuccess ? SPLASH_OK : SPLASH_ERR_CUDA;
 }
 

@@ -10,6 +10,8 @@
 // normalised by its own sum, lse_i) that lse_combine merges:
 //   lse = ln sum_i exp(lse_i),  O = sum_i exp(lse_i - lse) o_i
 // (an empty partial has lse_i = -inf and weight 0).
+#include <type_traits>
+
 #include "splash_common.cuh"
 
 namespace splash {
@@ -258,13 +260,23 @@ plan_kernel(const int32_t* __restrict__ context_lens, const int32_t* __restrict_
   }
 }
 
-// One warp per (token row, query head) of a split unit.
-template <int D>
+// WPR warps per (token row, query head) of a split unit; warp `sub` of a row
+// accumulates the partials j = sub, sub + WPR, ... (four or eight partial rows
+// in flight), and the WPR sums meet in shared memory. Every warp of a row reads all
+// lse_j in one pass (running max and rescaled sum per lane, then merged across
+// the warp), so the weights exp(lse_j - lse) agree across the row's warps.
+template <int D, int WPR>
 __global__ void __launch_bounds__(256)
 lse_combine_kernel(int num_q_tokens, int num_q_heads, int num_seqs, int num_kv_heads, int group,
                    int rows_bound, const unsigned char* __restrict__ ws,
                    __nv_bfloat16* __restrict__ out, float* __restrict__ lse_out) {
-  constexpr int EPL = D / 32;
+  constexpr int EPL = D / 32;                     // output columns per lane
+  constexpr int kRowsPerBlock = 8 / WPR;
+  constexpr int kUnroll = WPR >= 4 ? 8 : 4;      // partial rows in flight per warp
+  constexpr int VW = EPL >= 4 ? 4 : 2;           // floats per vector load
+  using Vec = typename std::conditional<VW == 4, float4, float2>::type;
+  static_assert(EPL % VW == 0, "vector loads of a lane's columns");
+  __shared__ float s_acc[WPR > 1 ? 8 : 1][WPR > 1 ? D : 1];
   grid_dependency_wait();          // the attention kernel's partials are complete
   const WorkspaceLayout L = make_layout(num_seqs, num_kv_heads, D, rows_bound);
   const int* q_off = reinterpret_cast<const int*>(ws + L.q_off);
@@ -273,59 +285,85 @@ lse_combine_kernel(int num_q_tokens, int num_q_heads, int num_seqs, int num_kv_h
   const int* part_base = reinterpret_cast<const int*>(ws + L.part_base);
   const float* o_part = reinterpret_cast<const float*>(ws + L.o_part);
   const float* lse_part = reinterpret_cast<const float*>(ws + L.lse_part);
-  const int lane = threadIdx.x & 31;
-  const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
-  if (row >= (long long)num_q_tokens * num_q_heads) return;
-  const int i = (int)(row / num_q_heads), hq = (int)(row % num_q_heads);
-  const int b = upper_index(q_off, num_seqs - 1, i);
-  const int h = hq / group, g = hq % group;
-  const int u = b * num_kv_heads + h;
-  const int n = nseg[u];
-  if (n <= 1 || i - q_off[b] >= seq_T[b]) return;
-  const int R = seq_T[b] * group;
-  const int r = (i - q_off[b]) * group + g;
-  const long long base = part_base[u];
-
-  // lse_i of the splits, 32 at a time across the lanes
-  float m = -INFINITY;
-  for (int j = lane; j < n; j += 32) m = fmaxf(m, lse_part[base + (long long)j * R + r]);
-  m = warp_max(m);
-  float wsum = 0.f;
-  for (int j = lane; j < n; j += 32) {
-    const float lj = lse_part[base + (long long)j * R + r];
-    wsum += (lj == -INFINITY) ? 0.f : __expf(lj - m);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, sub = warp % WPR;
+  const long long row = (long long)blockIdx.x * kRowsPerBlock + warp / WPR;
+  // the warp's row, when it belongs to a unit with two or more partials
+  bool active = row < (long long)num_q_tokens * num_q_heads;
+  int i = 0, hq = 0, n = 0, R = 0, r = 0;
+  long long base = 0;
+  if (active) {
+    i = (int)(row / num_q_heads);
+    hq = (int)(row % num_q_heads);
+    const int b = upper_index(q_off, num_seqs - 1, i);
+    const int h = hq / group, g = hq % group;
+    const int u = b * num_kv_heads + h;
+    n = nseg[u];
+    active = n > 1 && i - q_off[b] < seq_T[b];
+    R = seq_T[b] * group;
+    r = (i - q_off[b]) * group + g;
+    base = part_base[u];
   }
-  wsum = warp_sum(wsum);
-  // O: the partial rows of four splits are loaded before any is accumulated
   float acc[EPL];
 #pragma unroll
   for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
-  for (int j0 = 0; j0 < n; j0 += 4) {
-    float w[4];
-    float2 v[4][EPL / 2];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int j = j0 + k;
-      w[k] = 0.f;
-      if (j < n) {
-        const long long pr = base + (long long)j * R + r;
-        const float lj = lse_part[pr];
-        w[k] = (lj == -INFINITY) ? 0.f : __expf(lj - m);
-        const float* src = o_part + pr * D + lane * EPL;
-#pragma unroll
-        for (int e = 0; e < EPL / 2; ++e) v[k][e] = *reinterpret_cast<const float2*>(src + 2 * e);
+  float m = -INFINITY, wsum = 0.f;
+  if (active) {
+    // lse = m + ln(wsum) over all partials, one pass
+    float sl = 0.f;
+    for (int j = lane; j < n; j += 32) {
+      const float lj = lse_part[base + (long long)j * R + r];
+      if (lj > m) {
+        sl = sl * __expf(m - lj) + 1.f;     // m = -inf: sl is 0 and stays finite
+        m = lj;
+      } else if (lj != -INFINITY) {
+        sl += __expf(lj - m);
       }
     }
+    const float mw = warp_max(m);
+    wsum = warp_sum(m == -INFINITY ? 0.f : sl * __expf(m - mw));
+    m = mw;
+    for (int j0 = sub; j0 < n; j0 += kUnroll * WPR) {
+      float w[kUnroll];
+      Vec v[kUnroll][EPL / VW];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      if (w[k] == 0.f) continue;
+      for (int k = 0; k < kUnroll; ++k) {
+        const int j = j0 + k * WPR;
+        w[k] = 0.f;
+        if (j < n) {
+          const long long pr = base + (long long)j * R + r;
+          const float lj = lse_part[pr];
+          w[k] = (lj == -INFINITY) ? 0.f : __expf(lj - m);
+          const Vec* src = reinterpret_cast<const Vec*>(o_part + pr * D + lane * EPL);
 #pragma unroll
-      for (int e = 0; e < EPL / 2; ++e) {
-        acc[2 * e] = fmaf(w[k], v[k][e].x, acc[2 * e]);
-        acc[2 * e + 1] = fmaf(w[k], v[k][e].y, acc[2 * e + 1]);
+          for (int e = 0; e < EPL / VW; ++e) v[k][e] = src[e];
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < kUnroll; ++k) {
+        if (w[k] == 0.f) continue;
+#pragma unroll
+        for (int e = 0; e < EPL / VW; ++e) {
+          const float* x = reinterpret_cast<const float*>(&v[k][e]);
+#pragma unroll
+          for (int c = 0; c < VW; ++c) acc[VW * e + c] = fmaf(w[k], x[c], acc[VW * e + c]);
+        }
       }
     }
   }
+  if (WPR > 1) {
+    if (active) {
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) s_acc[warp][lane * EPL + e] = acc[e];
+    }
+    __syncthreads();
+    if (active && sub == 0) {
+#pragma unroll
+      for (int o = 1; o < WPR; ++o)
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) acc[e] += s_acc[warp + o][lane * EPL + e];
+    }
+  }
+  if (!active || sub != 0) return;
   const float inv = 1.f / wsum;
   __nv_bfloat16* dst = out + ((long long)i * num_q_heads + hq) * D + lane * EPL;
 #pragma unroll
@@ -347,21 +385,36 @@ cudaError_t launch_plan(const int32_t* context_lens, const int32_t* block_lens, 
 }
 
 cudaError_t launch_combine(int num_q_tokens, int num_q_heads, int num_seqs, int num_kv_heads,
-                           int group, int head_dim, int rows_bound, const unsigned char* ws,
-                           __nv_bfloat16* out, float* lse, cudaStream_t stream) {
+                           int group, int head_dim, int rows_bound, int sms,
+                           const unsigned char* ws, __nv_bfloat16* out, float* lse,
+                           cudaStream_t stream) {
   const long long rows = (long long)num_q_tokens * num_q_heads;
   if (rows == 0) return cudaSuccess;
-  const int grid = (int)((rows + 7) / 8);
-#define SPLASH_COMBINE(DD)                                                                     \
-  e = launch_dependent(lse_combine_kernel<DD>, dim3(grid), dim3(256), 0, stream, num_q_tokens, \
-                       num_q_heads, num_seqs, num_kv_heads, group, rows_bound, ws, out, lse)
-  cudaError_t e = cudaSuccess;
+  // warps per row: enough to give every SM about 16 warps when there are few
+  // rows (few rows means few units, each split over many CTAs)
+  const long long want = 16LL * (sms > 0 ? sms : 1);
+  const int wpr = rows * 4 <= want ? 8 : rows * 2 <= want ? 4 : rows <= want ? 2 : 1;
+  const long long rows_per_block = 8 / wpr;
+  const int grid = (int)((rows + rows_per_block - 1) / rows_per_block);
+  cudaError_t e = cudaErrorInvalidValue;
+#define SPLASH_COMBINE(DD, WW)                                                                  \
+  e = launch_dependent(lse_combine_kernel<DD, WW>, dim3(grid), dim3(256), 0, stream,            \
+                       num_q_tokens, num_q_heads, num_seqs, num_kv_heads, group, rows_bound, ws, \
+                       out, lse)
+#define SPLASH_COMBINE_D(DD)          \
+  switch (wpr) {                      \
+    case 1: SPLASH_COMBINE(DD, 1); break; \
+    case 2: SPLASH_COMBINE(DD, 2); break; \
+    case 4: SPLASH_COMBINE(DD, 4); break; \
+    default: SPLASH_COMBINE(DD, 8); break; \
+  }
   switch (head_dim) {
-    case 64: SPLASH_COMBINE(64); break;
-    case 128: SPLASH_COMBINE(128); break;
-    case 256: SPLASH_COMBINE(256); break;
+    case 64: SPLASH_COMBINE_D(64); break;
+    case 128: SPLASH_COMBINE_D(128); break;
+    case 256: SPLASH_COMBINE_D(256); break;
     default: return cudaErrorInvalidValue;
   }
+#undef SPLASH_COMBINE_D
 #undef SPLASH_COMBINE
   return e;
 }

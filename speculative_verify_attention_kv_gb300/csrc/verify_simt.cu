@@ -60,7 +60,6 @@ verify_simt_kernel(AttnParams p, int rows_cap) {
   float* o_part = reinterpret_cast<float*>(p.ws + L.o_part);
   float* lse_part = reinterpret_cast<float*>(p.ws + L.lse_part);
 
-  const int total = hd->total_tiles[kClassSimt];
   const int ncta = hd->ncta[kClassSimt];
   const int window = hd->window;
   if ((int)blockIdx.x >= ncta) return;

@@ -503,7 +503,6 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
   grid_dependency_wait();          // the split plan is complete
   allow_dependent_launch();
   const PlanHeader* hd = reinterpret_cast<const PlanHeader*>(p.ws);
-  const int total = hd->total_tiles[kClassTensor];
   const int ncta = hd->ncta[kClassTensor];
   if ((int)blockIdx.x >= ncta) return;
   // 128-byte swizzled operand tiles need a 1024-byte aligned base

@@ -259,7 +259,6 @@ verify_tt_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmap) {
   grid_dependency_wait();          // the split plan is complete
   allow_dependent_launch();
   const PlanHeader* hd = reinterpret_cast<const PlanHeader*>(p.ws);
-  const int total = hd->total_tiles[kClassTensor];
   const int ncta = hd->ncta[kClassTensor];
   if ((int)blockIdx.x >= ncta) return;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
