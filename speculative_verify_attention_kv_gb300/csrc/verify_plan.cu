@@ -17,6 +17,16 @@
 namespace splash {
 
 constexpr int kPlanThreads = 1024;
+// Batches up to this many sequences keep the planner's per-sequence arrays in
+// shared memory as well (the later passes read them back many times; from
+// global memory each read would cost an L2 round trip).
+constexpr int kPlanSmemSeqs = 1024;
+
+struct PlanSmem {
+  int T[kPlanSmemSeqs], ctx[kPlanSmemSeqs], cls[kPlanSmemSeqs];
+  int stp[kNumClasses][kPlanSmemSeqs + 1];
+  long long wcost[kNumClasses][kPlanSmemSeqs + 1];
+};
 
 // Inclusive max-scan over the CTA (kPlanThreads threads).
 __device__ inline int block_inclusive_max(int v, int* s_warp) {
@@ -80,7 +90,10 @@ plan_kernel(const int32_t* __restrict__ context_lens, const int32_t* __restrict_
   __shared__ int s_warp[32];
   __shared__ long long s_warp64[32];
   __shared__ int s_start[kNumClasses][kMaxCtas + 1];
+  extern __shared__ __align__(16) unsigned char s_dyn[];
   allow_dependent_launch();        // the attention kernel may get its SMs now
+  const bool small = num_seqs <= kPlanSmemSeqs;     // launched with sizeof(PlanSmem) then
+  PlanSmem* ps = reinterpret_cast<PlanSmem*>(s_dyn);
   const WorkspaceLayout L = make_layout(num_seqs, num_kv_heads, 0, rows_bound);
   int* q_off = reinterpret_cast<int*>(ws + L.q_off);
   int* seq_T = reinterpret_cast<int*>(ws + L.seq_T);
@@ -125,6 +138,11 @@ plan_kernel(const int32_t* __restrict__ context_lens, const int32_t* __restrict_
       seq_T[b] = T;
       seq_ctx[b] = ctx;
       seq_class[b] = cls;
+      if (small) {
+        ps->T[b] = T;
+        ps->ctx[b] = ctx;
+        ps->cls[b] = cls;
+      }
     }
     long long totq;
     const long long qo = block_exclusive_scan(rows_laid_out, s_warp64, &totq);
@@ -133,10 +151,16 @@ plan_kernel(const int32_t* __restrict__ context_lens, const int32_t* __restrict_
     run_q += totq;
     int tot;
     const int t0 = block_exclusive_scan(cls == 0 ? tiles * num_kv_heads : 0, s_warp, &tot);
-    if (b < num_seqs) stp[b] = run_t0 + t0;
+    if (b < num_seqs) {
+      stp[b] = run_t0 + t0;
+      if (small) ps->stp[0][b] = run_t0 + t0;
+    }
     run_t0 += tot;
     const int t1 = block_exclusive_scan(cls == 1 ? tiles * num_kv_heads : 0, s_warp, &tot);
-    if (b < num_seqs) stp[(num_seqs + 1) + b] = run_t1 + t1;
+    if (b < num_seqs) {
+      stp[(num_seqs + 1) + b] = run_t1 + t1;
+      if (small) ps->stp[1][b] = run_t1 + t1;
+    }
     run_t1 += tot;
     // estimated cost of the sequence's units, per class (see tile_cost)
 #pragma unroll
@@ -147,7 +171,10 @@ plan_kernel(const int32_t* __restrict__ context_lens, const int32_t* __restrict_
                    : 0;
       long long totw;
       const long long w0 = block_exclusive_scan(cost, s_warp64, &totw);
-      if (b < num_seqs) wcost[c * (num_seqs + 1) + b] = run_w[c] + w0;
+      if (b < num_seqs) {
+        wcost[c * (num_seqs + 1) + b] = run_w[c] + w0;
+        if (small) ps->wcost[c][b] = run_w[c] + w0;
+      }
       run_w[c] += totw;
     }
   }
@@ -156,14 +183,25 @@ plan_kernel(const int32_t* __restrict__ context_lens, const int32_t* __restrict_
     stp[num_seqs] = run_t0;
     stp[(num_seqs + 1) + num_seqs] = run_t1;
     for (int c = 0; c < kNumClasses; ++c) wcost[c * (num_seqs + 1) + num_seqs] = run_w[c];
+    if (small) {
+      ps->stp[0][num_seqs] = run_t0;
+      ps->stp[1][num_seqs] = run_t1;
+      for (int c = 0; c < kNumClasses; ++c) ps->wcost[c][num_seqs] = run_w[c];
+    }
   }
   __syncthreads();
+  // where the later passes read the per-sequence arrays
+  const int* rT = small ? ps->T : seq_T;
+  const int* rctx = small ? ps->ctx : seq_ctx;
   // block lengths that sum past the q / out rows the caller passed: do nothing
   const bool rows_ok = run_q <= num_q_tokens;
   if (!rows_ok) {
     if (threadIdx.x == 0) report(device_status, SPLASH_DEVICE_BAD_LENGTH);
     run_t0 = run_t1 = 0;
-    for (int b = threadIdx.x; b < num_seqs; b += kPlanThreads) seq_class[b] = -1;
+    for (int b = threadIdx.x; b < num_seqs; b += kPlanThreads) {
+      seq_class[b] = -1;
+      if (small) ps->cls[b] = -1;
+    }
     __syncthreads();
   }
   const int total[kNumClasses] = {run_t0, run_t1};
@@ -179,8 +217,8 @@ plan_kernel(const int32_t* __restrict__ context_lens, const int32_t* __restrict_
   // last ones are pulled back so that CTA n - 1 still fits before `total`.
   for (int c = 0; c < kNumClasses; ++c) {
     const int n = ncta_eff[c];
-    const long long* wc = wcost + c * (num_seqs + 1);
-    const int* sp = stp + c * (num_seqs + 1);
+    const long long* wc = small ? ps->wcost[c] : wcost + c * (num_seqs + 1);
+    const int* sp = small ? ps->stp[c] : stp + c * (num_seqs + 1);
     static_assert(kMaxCtas + 1 <= kPlanThreads, "one start per planner thread");
     {
       const int k = threadIdx.x;
@@ -192,8 +230,8 @@ plan_kernel(const int32_t* __restrict__ context_lens, const int32_t* __restrict_
           const long long target = run_w[c] * k / n;      // < 2^63 for any realistic batch
           const int b = upper_index(wc, num_seqs - 1, target);
           const long long off = target - wc[b];
-          const int T = seq_T[b];
-          const int tiles = unit_tiles(seq_ctx[b], T, window, tile[c]);
+          const int T = rT[b];
+          const int tiles = unit_tiles(rctx[b], T, window, tile[c]);
           const long long w = tile_cost(c) + row_cost(c) * T * group;
           const long long uc = (long long)tiles * w + segment_cost(c);
           const int h = (int)min(off / uc, (long long)num_kv_heads - 1);
@@ -221,14 +259,14 @@ plan_kernel(const int32_t* __restrict__ context_lens, const int32_t* __restrict_
     int rows = 0;
     if (u < num_units) {
       const int b = u / num_kv_heads, h = u % num_kv_heads;
-      const int cls = seq_class[b];
+      const int cls = small ? ps->cls[b] : seq_class[b];
       int ns = 0, cf = 0;
       if (cls >= 0) {
-        const int T = seq_T[b], ctx = seq_ctx[b];
+        const int T = rT[b], ctx = rctx[b];
         const int tk = cls == 0 ? tile[0] : tile[1];        // selects, not a local-memory index
         const int nce = cls == 0 ? ncta_eff[0] : ncta_eff[1];
         const int tiles = unit_tiles(ctx, T, window, tk);
-        const int tp = stp[cls * (num_seqs + 1) + b] + h * tiles;
+        const int tp = (small ? ps->stp[cls][b] : stp[cls * (num_seqs + 1) + b]) + h * tiles;
         const int* cs = s_start[cls == 0 ? 0 : 1];
         cf = upper_index(cs, nce - 1, tp);
         const int cl = upper_index(cs, nce - 1, tp + tiles - 1);
@@ -377,7 +415,8 @@ cudaError_t launch_plan(const int32_t* context_lens, const int32_t* block_lens, 
                         int tile_simt, int ncta_tc, int ncta_simt, int path, int rows_bound,
                         int num_q_tokens, int window, unsigned char* ws, int* device_status,
                         cudaStream_t stream) {
-  plan_kernel<<<1, kPlanThreads, 0, stream>>>(context_lens, block_lens, num_seqs, num_kv_heads,
+  const size_t dyn = num_seqs <= kPlanSmemSeqs ? sizeof(PlanSmem) : 0;
+  plan_kernel<<<1, kPlanThreads, dyn, stream>>>(context_lens, block_lens, num_seqs, num_kv_heads,
                                               group, max_pages, max_block_len, tile_tc, tile_simt,
                                               ncta_tc, ncta_simt, path, rows_bound, num_q_tokens,
                                               window, ws, device_status);

@@ -500,11 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
   using C = Cfg<D>;
   static_assert(sizeof(Smem) <= C::kBarBytes, "barrier area");
   extern __shared__ uint8_t smem_raw[];
-  grid_dependency_wait();          // the split plan is complete
   allow_dependent_launch();
-  const PlanHeader* hd = reinterpret_cast<const PlanHeader*>(p.ws);
-  const int ncta = hd->ncta[kClassTensor];
-  if ((int)blockIdx.x >= ncta) return;
   // 128-byte swizzled operand tiles need a 1024-byte aligned base
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -519,17 +515,6 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
   Smem* sh = reinterpret_cast<Smem*>(smem + C::kOffBars);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int B = p.num_seqs, Hkv = p.num_kv_heads, G = p.group;
-  const WorkspaceLayout L = make_layout(B, Hkv, D, hd->rows_bound);
-  const int* q_off = reinterpret_cast<const int*>(p.ws + L.q_off);
-  const int* seq_T = reinterpret_cast<const int*>(p.ws + L.seq_T);
-  const int* seq_ctx = reinterpret_cast<const int*>(p.ws + L.seq_ctx);
-  const int* stp = reinterpret_cast<const int*>(p.ws + L.stp) + kClassTensor * (B + 1);
-  const int* nseg = reinterpret_cast<const int*>(p.ws + L.nseg);
-  const int* cfirst = reinterpret_cast<const int*>(p.ws + L.cfirst);
-  const int* part_base = reinterpret_cast<const int*>(p.ws + L.part_base);
-  float* o_part = reinterpret_cast<float*>(p.ws + L.o_part);
-  float* lse_part = reinterpret_cast<float*>(p.ws + L.lse_part);
 
   if (tid == 0) {
     for (int s = 0; s < kRing; ++s) {
@@ -567,6 +552,27 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
   fence_after();
   const uint32_t tmem = sh->tmem_base;
   const Sync sync{&sh->abort_flag, p.device_status, p.wait_ns};
+
+  // the set-up above overlaps the planner; from here on the plan is read
+  grid_dependency_wait();
+  const PlanHeader* hd = reinterpret_cast<const PlanHeader*>(p.ws);
+  if ((int)blockIdx.x >= hd->ncta[kClassTensor]) {         // no tiles for this CTA
+    if (warp == kMmaWarp)
+      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                   "r"(kTmemCols) : "memory");
+    return;
+  }
+  const int B = p.num_seqs, Hkv = p.num_kv_heads, G = p.group;
+  const WorkspaceLayout L = make_layout(B, Hkv, D, hd->rows_bound);
+  const int* q_off = reinterpret_cast<const int*>(p.ws + L.q_off);
+  const int* seq_T = reinterpret_cast<const int*>(p.ws + L.seq_T);
+  const int* seq_ctx = reinterpret_cast<const int*>(p.ws + L.seq_ctx);
+  const int* stp = reinterpret_cast<const int*>(p.ws + L.stp) + kClassTensor * (B + 1);
+  const int* nseg = reinterpret_cast<const int*>(p.ws + L.nseg);
+  const int* cfirst = reinterpret_cast<const int*>(p.ws + L.cfirst);
+  const int* part_base = reinterpret_cast<const int*>(p.ws + L.part_base);
+  float* o_part = reinterpret_cast<float*>(p.ws + L.o_part);
+  float* lse_part = reinterpret_cast<float*>(p.ws + L.lse_part);
 
   const int window = kSwa ? p.window : 0;
   const int* cst = reinterpret_cast<const int*>(p.ws + L.cta_start) + kClassTensor * (kMaxCtas + 1);
