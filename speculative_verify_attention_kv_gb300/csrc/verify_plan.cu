@@ -28,28 +28,75 @@ struct PlanSmem {
   long long wcost[kNumClasses][kPlanSmemSeqs + 1];
 };
 
-// Inclusive max-scan over the CTA (kPlanThreads threads).
-__device__ inline int block_inclusive_max(int v, int* s_warp) {
+// Inclusive max-scans of two values over the CTA (kPlanThreads threads).
+__device__ inline int2 block_inclusive_max2(int2 v, int2* s_warp) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int incl = v;
+  int2 incl = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    int y = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl = max(incl, y);
+    const int y0 = __shfl_up_sync(0xffffffffu, incl.x, o);
+    const int y1 = __shfl_up_sync(0xffffffffu, incl.y, o);
+    if (lane >= o) incl = make_int2(max(incl.x, y0), max(incl.y, y1));
   }
   if (lane == 31) s_warp[warp] = incl;
   __syncthreads();
   if (warp == 0) {
-    int x = s_warp[lane];
+    int2 x = s_warp[lane];
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      int y = __shfl_up_sync(0xffffffffu, x, o);
-      if (lane >= o) x = max(x, y);
+      const int y0 = __shfl_up_sync(0xffffffffu, x.x, o);
+      const int y1 = __shfl_up_sync(0xffffffffu, x.y, o);
+      if (lane >= o) x = make_int2(max(x.x, y0), max(x.y, y1));
     }
     s_warp[lane] = x;
   }
   __syncthreads();
-  const int res = warp ? max(s_warp[warp - 1], incl) : incl;
+  int2 res = incl;
+  if (warp) res = make_int2(max(s_warp[warp - 1].x, incl.x), max(s_warp[warp - 1].y, incl.y));
+  __syncthreads();
+  return res;
+}
+
+// The per-sequence quantities pass 1 sums: Q/O rows laid out, key tiles and
+// estimated cost per class.
+struct PlanSums {
+  long long q, w0, w1;
+  int t0, t1;
+  __device__ PlanSums operator+(const PlanSums& o) const {
+    return PlanSums{q + o.q, w0 + o.w0, w1 + o.w1, t0 + o.t0, t1 + o.t1};
+  }
+};
+__device__ inline PlanSums shfl_up(const PlanSums& v, int o) {
+  return PlanSums{__shfl_up_sync(0xffffffffu, v.q, o), __shfl_up_sync(0xffffffffu, v.w0, o),
+                  __shfl_up_sync(0xffffffffu, v.w1, o), __shfl_up_sync(0xffffffffu, v.t0, o),
+                  __shfl_up_sync(0xffffffffu, v.t1, o)};
+}
+
+// Exclusive scan of PlanSums over the CTA (one set of barriers for all five).
+__device__ inline PlanSums block_exclusive_scan_sums(PlanSums v, PlanSums* s_warp, PlanSums* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  PlanSums incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const PlanSums y = shfl_up(incl, o);
+    if (lane >= o) incl = incl + y;
+  }
+  if (lane == 31) s_warp[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    PlanSums x = s_warp[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const PlanSums y = shfl_up(x, o);
+      if (lane >= o) x = x + y;
+    }
+    s_warp[lane] = x;
+  }
+  __syncthreads();
+  const PlanSums zero{0, 0, 0, 0, 0};
+  PlanSums res = (warp ? s_warp[warp - 1] : zero) + incl;
+  res = PlanSums{res.q - v.q, res.w0 - v.w0, res.w1 - v.w1, res.t0 - v.t0, res.t1 - v.t1};
+  *total = s_warp[31];
   __syncthreads();
   return res;
 }
@@ -88,7 +135,8 @@ plan_kernel(const int32_t* __restrict__ context_lens, const int32_t* __restrict_
             int tile_tc, int tile_simt, int ncta_tc, int ncta_simt, int path, int rows_bound,
             int num_q_tokens, int window, unsigned char* ws, int* device_status) {
   __shared__ int s_warp[32];
-  __shared__ long long s_warp64[32];
+  __shared__ int2 s_warp2[32];
+  __shared__ PlanSums s_sums[32];
   __shared__ int s_start[kNumClasses][kMaxCtas + 1];
   extern __shared__ __align__(16) unsigned char s_dyn[];
   allow_dependent_launch();        // the attention kernel may get its SMs now
@@ -144,39 +192,34 @@ plan_kernel(const int32_t* __restrict__ context_lens, const int32_t* __restrict_
         ps->cls[b] = cls;
       }
     }
-    long long totq;
-    const long long qo = block_exclusive_scan(rows_laid_out, s_warp64, &totq);
-    // offsets past the caller's rows only occur when the plan is dropped below
-    if (b < num_seqs) q_off[b] = (int)min(run_q + qo, (long long)num_q_tokens);
-    run_q += totq;
-    int tot;
-    const int t0 = block_exclusive_scan(cls == 0 ? tiles * num_kv_heads : 0, s_warp, &tot);
+    // estimated cost of the sequence's units in its class (see tile_cost)
+    long long cost = 0;
+    if (cls >= 0)
+      cost = (long long)num_kv_heads *
+             ((long long)tiles * (tile_cost(cls) + row_cost(cls) * T * group) + segment_cost(cls));
+    const PlanSums mine{rows_laid_out, cls == 0 ? cost : 0, cls == 1 ? cost : 0,
+                        cls == 0 ? tiles * num_kv_heads : 0, cls == 1 ? tiles * num_kv_heads : 0};
+    PlanSums tot;
+    const PlanSums ex = block_exclusive_scan_sums(mine, s_sums, &tot);
     if (b < num_seqs) {
-      stp[b] = run_t0 + t0;
-      if (small) ps->stp[0][b] = run_t0 + t0;
-    }
-    run_t0 += tot;
-    const int t1 = block_exclusive_scan(cls == 1 ? tiles * num_kv_heads : 0, s_warp, &tot);
-    if (b < num_seqs) {
-      stp[(num_seqs + 1) + b] = run_t1 + t1;
-      if (small) ps->stp[1][b] = run_t1 + t1;
-    }
-    run_t1 += tot;
-    // estimated cost of the sequence's units, per class (see tile_cost)
-#pragma unroll
-    for (int c = 0; c < kNumClasses; ++c) {
-      const long long cost =
-          cls == c ? (long long)num_kv_heads *
-                         ((long long)tiles * (tile_cost(c) + row_cost(c) * T * group) + segment_cost(c))
-                   : 0;
-      long long totw;
-      const long long w0 = block_exclusive_scan(cost, s_warp64, &totw);
-      if (b < num_seqs) {
-        wcost[c * (num_seqs + 1) + b] = run_w[c] + w0;
-        if (small) ps->wcost[c][b] = run_w[c] + w0;
+      // offsets past the caller's rows only occur when the plan is dropped below
+      q_off[b] = (int)min(run_q + ex.q, (long long)num_q_tokens);
+      stp[b] = run_t0 + ex.t0;
+      stp[(num_seqs + 1) + b] = run_t1 + ex.t1;
+      wcost[b] = run_w[0] + ex.w0;
+      wcost[(num_seqs + 1) + b] = run_w[1] + ex.w1;
+      if (small) {
+        ps->stp[0][b] = run_t0 + ex.t0;
+        ps->stp[1][b] = run_t1 + ex.t1;
+        ps->wcost[0][b] = run_w[0] + ex.w0;
+        ps->wcost[1][b] = run_w[1] + ex.w1;
       }
-      run_w[c] += totw;
     }
+    run_q += tot.q;
+    run_t0 += tot.t0;
+    run_t1 += tot.t1;
+    run_w[0] += tot.w0;
+    run_w[1] += tot.w1;
   }
   if (threadIdx.x == 0) {
     q_off[num_seqs] = (int)min(run_q, (long long)num_q_tokens);
@@ -215,17 +258,18 @@ plan_kernel(const int32_t* __restrict__ context_lens, const int32_t* __restrict_
   // tile (the first segment_cost of a unit maps to its first tile). Then the
   // starts are made strictly increasing (every CTA owns >= 1 tile) and the
   // last ones are pulled back so that CTA n - 1 still fits before `total`.
-  for (int c = 0; c < kNumClasses; ++c) {
-    const int n = ncta_eff[c];
-    const long long* wc = small ? ps->wcost[c] : wcost + c * (num_seqs + 1);
-    const int* sp = small ? ps->stp[c] : stp + c * (num_seqs + 1);
-    static_assert(kMaxCtas + 1 <= kPlanThreads, "one start per planner thread");
-    {
-      const int k = threadIdx.x;
-      int start = 0;
+  static_assert(kMaxCtas + 1 <= kPlanThreads, "one start per planner thread");
+  {
+    const int k = threadIdx.x;
+    int start[kNumClasses] = {0, 0};
+#pragma unroll
+    for (int c = 0; c < kNumClasses; ++c) {
+      const int n = ncta_eff[c];
+      const long long* wc = small ? ps->wcost[c] : wcost + c * (num_seqs + 1);
+      const int* sp = small ? ps->stp[c] : stp + c * (num_seqs + 1);
       if (k <= n && n > 0 && rows_ok) {
         if (k == n) {
-          start = total[c];
+          start[c] = total[c];
         } else if (k > 0) {
           const long long target = run_w[c] * k / n;      // < 2^63 for any realistic batch
           const int b = upper_index(wc, num_seqs - 1, target);
@@ -237,14 +281,16 @@ plan_kernel(const int32_t* __restrict__ context_lens, const int32_t* __restrict_
           const int h = (int)min(off / uc, (long long)num_kv_heads - 1);
           const long long rem = off - h * uc;
           const int t = rem < segment_cost(c) ? 0 : (int)min((rem - segment_cost(c)) / w, (long long)tiles - 1);
-          start = sp[b] + h * tiles + t;
+          start[c] = sp[b] + h * tiles + t;
         }
       }
-      // strictly increasing: prefix max of start - k, plus k
-      const int y = block_inclusive_max(k <= n ? start - k : -(1 << 30), s_warp);
-      if (k <= n) s_start[c][k] = min(y + k, total[c] - (n - k));
-      __syncthreads();
     }
+    // strictly increasing: prefix max of start - k, plus k (both classes at once)
+    const int2 y = block_inclusive_max2(
+        make_int2(k <= ncta_eff[0] ? start[0] - k : -(1 << 30), k <= ncta_eff[1] ? start[1] - k : -(1 << 30)),
+        s_warp2);
+    if (k <= ncta_eff[0]) s_start[0][k] = min(y.x + k, total[0] - (ncta_eff[0] - k));
+    if (k <= ncta_eff[1]) s_start[1][k] = min(y.y + k, total[1] - (ncta_eff[1] - k));
   }
   __syncthreads();
   for (int c = 0; c < kNumClasses; ++c)
@@ -304,7 +350,7 @@ plan_kernel(const int32_t* __restrict__ context_lens, const int32_t* __restrict_
 // lse_j in one pass (running max and rescaled sum per lane, then merged across
 // the warp), so the weights exp(lse_j - lse) agree across the row's warps.
 template <int D, int WPR>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, 2)
 lse_combine_kernel(int num_q_tokens, int num_q_heads, int num_seqs, int num_kv_heads, int group,
                    int rows_bound, const unsigned char* __restrict__ ws,
                    __nv_bfloat16* __restrict__ out, float* __restrict__ lse_out) {
