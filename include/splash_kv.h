@@ -37,6 +37,13 @@
  *                      codes of a (page, KV head) are one contiguous 2*P*D-byte
  *                      block. k_pages points at the pool, v_pages must equal
  *                      k_pages + P*D (anything else is SPLASH_ERR_INVALID_ARGUMENT).
+ *                      v_pages is therefore fixed by k_pages: it carries no
+ *                      information of its own, and separate K and V pools (the
+ *                      layout of a two-pool cache) cannot be passed. The
+ *                      interleaving lets one bulk copy move a (page, KV head)'s
+ *                      K and V codes together; a copy's issue cost is mostly
+ *                      per copy, and the same attention ran 6.8% faster than
+ *                      with two pools of 4 KB copies at D = 256.
  *                      Slot s of (page, h): k_pages[((page*Hkv + h)*2*P + s)*D + d],
  *                      and the same offset from v_pages.
  *   k_scales, v_scales: fp32 [num_pages, Hkv, P]      one scale per (token, KV head)
@@ -178,6 +185,14 @@ size_t splash_verify_attention_workspace_size(int num_seqs, int num_q_tokens, in
  * splash_verify_attention — block-causal attention of every verify token over
  * its sequence's int8 paged cache (the block itself already appended).
  *
+ * The target model checks a sequence's whole draft block in one forward pass
+ * (Splash article on discuss.pytorch.kr, section "옵션이 아니라 기본 경로인
+ * DFlash 2 추측 디코딩"); the kernel reads the 8-bit cache directly and serves
+ * the G query heads of a KV head and the T verify tokens from each KV tile it
+ * loads (section "형상에 맞춰 자동으로 생성하는 Metal 커널"). The mask that lets
+ * verify token t see the block's tokens 0..t is this library's reading: the
+ * pages do not state one.
+ *
  * Verify token t of sequence b, query head hq (KV head h = hq / G) attends to
  * logical keys j = 0 .. context_lens[b] + t inclusive, dequantised as
  * code * scale:
@@ -186,7 +201,8 @@ size_t splash_verify_attention_workspace_size(int num_seqs, int num_q_tokens, in
  *   lse     = ln sum_j exp(score_j)   (sm_scale included)   -> fp32
  * q, out: bf16 bit patterns [num_q_tokens, Hq, D]; lse: fp32 [num_q_tokens, Hq].
  * num_q_tokens = sum(block_lens). max_block_len bounds every T_b (T_b * G must
- * be <= 128). sm_scale must be finite and > 0. The KV range of every sequence is split across CTAs; partials
+ * be <= 128). sm_scale must be finite and > 0. The KV range of every
+ * sequence is split across CTAs; partials
  * are merged by log-sum-exp in `workspace` (>= the size query's bytes, 256-byte
  * aligned). Deterministic: a fixed input, device and argument list gives
  * bitwise identical outputs, independent of the physical page numbering.
@@ -205,9 +221,17 @@ int splash_verify_attention(const uint16_t* q, int num_q_tokens,
  * splash_verify_attention_tuned — splash_verify_attention with the kernel
  * choice and the split granularity fixed by the caller (tests, benchmarks).
  *   path: 0 automatic; 1 CUDA-core kernel for every sequence; 2 tensor-core
- *         kernel for every sequence.
- *   ctas_per_class: 0 automatic (fills the GPU); n > 0 uses n persistent CTAs
- *         per kernel (1 = every sequence's KV range handled unsplit).
+ *         kernel for every sequence; 3 the transposed tensor-core kernel
+ *         (S^T = K Q'^T: keys on the MMA's M side, no row padding) for every
+ *         sequence, only at head_dim 256 with T * G <= 96
+ *         (SPLASH_ERR_UNSUPPORTED otherwise). Path 3 exists for comparison:
+ *         it is slower than path 2 on every workload measured.
+ *   ctas_per_class: 0 automatic (fills the GPU); 0 < n <= 1023 uses n
+ *         persistent CTAs per kernel (1 = every sequence's KV range handled
+ *         unsplit); larger n is SPLASH_ERR_INVALID_ARGUMENT. The planner
+ *         splits each kernel's stream of key tiles over its CTAs by estimated
+ *         cost (a tile of a unit with more query rows costs more; every unit
+ *         start adds one pipeline fill), from the lengths alone.
  * Same result contract as splash_verify_attention (within rounding across
  * different choices; bitwise for a fixed choice).
  */
