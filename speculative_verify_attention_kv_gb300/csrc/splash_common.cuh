@@ -6,6 +6,8 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "splash_kv.h"
 
 namespace splash {
@@ -145,6 +147,26 @@ __device__ __forceinline__ void grid_dependency_wait() {
 __device__ __forceinline__ void allow_dependent_launch() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
+// Raises kernel K's dynamic shared-memory limit to `bytes` on the current
+// device, calling the driver only the first time (and when a larger size is
+// asked for): the attribute is per device and persists, and one driver call
+// per launch would be host time on every call.
+template <auto K>
+inline cudaError_t ensure_dynamic_smem(int bytes) {
+  static std::mutex mu;
+  static int set_to[64] = {0};        // largest size set so far, per device
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64)
+    return cudaFuncSetAttribute(K, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  std::lock_guard<std::mutex> lock(mu);
+  if (set_to[dev] >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(K, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) set_to[dev] = bytes;
+  return e;
+}
+
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
                                     cudaStream_t stream, Args... args) {

@@ -10,13 +10,20 @@
 // normalised by its own sum, lse_i) that lse_combine merges:
 //   lse = ln sum_i exp(lse_i),  O = sum_i exp(lse_i - lse) o_i
 // (an empty partial has lse_i = -inf and weight 0).
+#include <climits>
 #include <type_traits>
 
 #include "splash_common.cuh"
 
 namespace splash {
 
-constexpr int kPlanThreads = 1024;
+// The planner runs as one CTA of kPlanThreadsLarge threads, or of
+// kPlanThreadsSmall for batches of at most kPlanSmallSeqs sequences (fewer
+// warps make its many block-wide barriers cheaper; every pass loops over its
+// items in chunks of the block size).
+constexpr int kPlanThreadsLarge = 1024;
+constexpr int kPlanThreadsSmall = 128;
+constexpr int kPlanSmallSeqs = 128;
 // Batches up to this many sequences keep the planner's per-sequence arrays in
 // shared memory as well (the later passes read them back many times; from
 // global memory each read would cost an L2 round trip).
@@ -28,9 +35,9 @@ struct PlanSmem {
   long long wcost[kNumClasses][kPlanSmemSeqs + 1];
 };
 
-// Inclusive max-scans of two values over the CTA (kPlanThreads threads).
+// Inclusive max-scans of two values over the CTA (any multiple of 32 threads).
 __device__ inline int2 block_inclusive_max2(int2 v, int2* s_warp) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
   int2 incl = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -41,7 +48,7 @@ __device__ inline int2 block_inclusive_max2(int2 v, int2* s_warp) {
   if (lane == 31) s_warp[warp] = incl;
   __syncthreads();
   if (warp == 0) {
-    int2 x = s_warp[lane];
+    int2 x = lane < nw ? s_warp[lane] : make_int2(INT_MIN, INT_MIN);
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int y0 = __shfl_up_sync(0xffffffffu, x.x, o);
@@ -74,7 +81,8 @@ __device__ inline PlanSums shfl_up(const PlanSums& v, int o) {
 
 // Exclusive scan of PlanSums over the CTA (one set of barriers for all five).
 __device__ inline PlanSums block_exclusive_scan_sums(PlanSums v, PlanSums* s_warp, PlanSums* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const PlanSums zero{0, 0, 0, 0, 0};
   PlanSums incl = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -84,7 +92,7 @@ __device__ inline PlanSums block_exclusive_scan_sums(PlanSums v, PlanSums* s_war
   if (lane == 31) s_warp[warp] = incl;
   __syncthreads();
   if (warp == 0) {
-    PlanSums x = s_warp[lane];
+    PlanSums x = lane < nw ? s_warp[lane] : zero;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const PlanSums y = shfl_up(x, o);
@@ -93,18 +101,17 @@ __device__ inline PlanSums block_exclusive_scan_sums(PlanSums v, PlanSums* s_war
     s_warp[lane] = x;
   }
   __syncthreads();
-  const PlanSums zero{0, 0, 0, 0, 0};
   PlanSums res = (warp ? s_warp[warp - 1] : zero) + incl;
   res = PlanSums{res.q - v.q, res.w0 - v.w0, res.w1 - v.w1, res.t0 - v.t0, res.t1 - v.t1};
-  *total = s_warp[31];
+  *total = s_warp[nw - 1];
   __syncthreads();
   return res;
 }
 
-// Exclusive scan over the CTA (kPlanThreads threads); *total receives the sum.
+// Exclusive scan over the CTA (any multiple of 32 threads); *total receives the sum.
 template <typename V>
 __device__ inline V block_exclusive_scan(V v, V* s_warp, V* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
   V incl = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -114,7 +121,7 @@ __device__ inline V block_exclusive_scan(V v, V* s_warp, V* total) {
   if (lane == 31) s_warp[warp] = incl;
   __syncthreads();
   if (warp == 0) {
-    V x = s_warp[lane];
+    V x = lane < nw ? s_warp[lane] : V(0);
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       V y = __shfl_up_sync(0xffffffffu, x, o);
@@ -124,12 +131,12 @@ __device__ inline V block_exclusive_scan(V v, V* s_warp, V* total) {
   }
   __syncthreads();
   const V res = (warp ? s_warp[warp - 1] : V(0)) + incl - v;
-  *total = s_warp[31];
+  *total = s_warp[nw - 1];
   __syncthreads();
   return res;
 }
 
-__global__ void __launch_bounds__(kPlanThreads)
+__global__ void __launch_bounds__(kPlanThreadsLarge)
 plan_kernel(const int32_t* __restrict__ context_lens, const int32_t* __restrict__ block_lens,
             int num_seqs, int num_kv_heads, int group, int max_pages, int max_block_len,
             int tile_tc, int tile_simt, int ncta_tc, int ncta_simt, int path, int rows_bound,
@@ -162,7 +169,7 @@ plan_kernel(const int32_t* __restrict__ context_lens, const int32_t* __restrict_
   // a rejected sequence is idle, and the others keep their rows.
   long long run_q = 0, run_w[kNumClasses] = {0, 0};
   int run_t0 = 0, run_t1 = 0;
-  for (int base = 0; base < num_seqs; base += kPlanThreads) {
+  for (int base = 0; base < num_seqs; base += (int)blockDim.x) {
     const int b = base + threadIdx.x;
     int T = 0, ctx = 0, cls = -1, tiles = 0;
     long long rows_laid_out = 0;
@@ -241,7 +248,7 @@ plan_kernel(const int32_t* __restrict__ context_lens, const int32_t* __restrict_
   if (!rows_ok) {
     if (threadIdx.x == 0) report(device_status, SPLASH_DEVICE_BAD_LENGTH);
     run_t0 = run_t1 = 0;
-    for (int b = threadIdx.x; b < num_seqs; b += kPlanThreads) {
+    for (int b = threadIdx.x; b < num_seqs; b += blockDim.x) {
       seq_class[b] = -1;
       if (small) ps->cls[b] = -1;
     }
@@ -258,49 +265,60 @@ plan_kernel(const int32_t* __restrict__ context_lens, const int32_t* __restrict_
   // tile (the first segment_cost of a unit maps to its first tile). Then the
   // starts are made strictly increasing (every CTA owns >= 1 tile) and the
   // last ones are pulled back so that CTA n - 1 still fits before `total`.
-  static_assert(kMaxCtas + 1 <= kPlanThreads, "one start per planner thread");
+  // one CTA start per thread, in chunks of the block size; the prefix max
+  // carries from chunk to chunk
   {
-    const int k = threadIdx.x;
-    int start[kNumClasses] = {0, 0};
+    int2 carry = make_int2(INT_MIN, INT_MIN);
+    const int kmax = max(ncta_eff[0], ncta_eff[1]);
+    for (int base = 0; base <= kmax; base += (int)blockDim.x) {
+      const int k = base + threadIdx.x;
+      int start[kNumClasses] = {0, 0};
 #pragma unroll
-    for (int c = 0; c < kNumClasses; ++c) {
-      const int n = ncta_eff[c];
-      const long long* wc = small ? ps->wcost[c] : wcost + c * (num_seqs + 1);
-      const int* sp = small ? ps->stp[c] : stp + c * (num_seqs + 1);
-      if (k <= n && n > 0 && rows_ok) {
-        if (k == n) {
-          start[c] = total[c];
-        } else if (k > 0) {
-          const long long target = run_w[c] * k / n;      // < 2^63 for any realistic batch
-          const int b = upper_index(wc, num_seqs - 1, target);
-          const long long off = target - wc[b];
-          const int T = rT[b];
-          const int tiles = unit_tiles(rctx[b], T, window, tile[c]);
-          const long long w = tile_cost(c) + row_cost(c) * T * group;
-          const long long uc = (long long)tiles * w + segment_cost(c);
-          const int h = (int)min(off / uc, (long long)num_kv_heads - 1);
-          const long long rem = off - h * uc;
-          const int t = rem < segment_cost(c) ? 0 : (int)min((rem - segment_cost(c)) / w, (long long)tiles - 1);
-          start[c] = sp[b] + h * tiles + t;
+      for (int c = 0; c < kNumClasses; ++c) {
+        const int n = ncta_eff[c];
+        const long long* wc = small ? ps->wcost[c] : wcost + c * (num_seqs + 1);
+        const int* sp = small ? ps->stp[c] : stp + c * (num_seqs + 1);
+        if (k <= n && n > 0 && rows_ok) {
+          if (k == n) {
+            start[c] = total[c];
+          } else if (k > 0) {
+            const long long target = run_w[c] * k / n;      // < 2^63 for any realistic batch
+            const int b = upper_index(wc, num_seqs - 1, target);
+            const long long off = target - wc[b];
+            const int T = rT[b];
+            const int tiles = unit_tiles(rctx[b], T, window, tile[c]);
+            const long long w = tile_cost(c) + row_cost(c) * T * group;
+            const long long uc = (long long)tiles * w + segment_cost(c);
+            const int h = (int)min(off / uc, (long long)num_kv_heads - 1);
+            const long long rem = off - h * uc;
+            const int t = rem < segment_cost(c) ? 0 : (int)min((rem - segment_cost(c)) / w, (long long)tiles - 1);
+            start[c] = sp[b] + h * tiles + t;
+          }
         }
       }
+      // strictly increasing: prefix max of start - k, plus k (both classes at once)
+      int2 y = block_inclusive_max2(make_int2(k <= ncta_eff[0] ? start[0] - k : INT_MIN,
+                                              k <= ncta_eff[1] ? start[1] - k : INT_MIN),
+                                    s_warp2);
+      y = make_int2(max(y.x, carry.x), max(y.y, carry.y));
+      if (k <= ncta_eff[0]) s_start[0][k] = min(y.x + k, total[0] - (ncta_eff[0] - k));
+      if (k <= ncta_eff[1]) s_start[1][k] = min(y.y + k, total[1] - (ncta_eff[1] - k));
+      // this chunk's maximum (the last thread's inclusive value) carries on
+      if (threadIdx.x == blockDim.x - 1) s_warp2[0] = y;
+      __syncthreads();
+      carry = s_warp2[0];
+      __syncthreads();
     }
-    // strictly increasing: prefix max of start - k, plus k (both classes at once)
-    const int2 y = block_inclusive_max2(
-        make_int2(k <= ncta_eff[0] ? start[0] - k : -(1 << 30), k <= ncta_eff[1] ? start[1] - k : -(1 << 30)),
-        s_warp2);
-    if (k <= ncta_eff[0]) s_start[0][k] = min(y.x + k, total[0] - (ncta_eff[0] - k));
-    if (k <= ncta_eff[1]) s_start[1][k] = min(y.y + k, total[1] - (ncta_eff[1] - k));
   }
   __syncthreads();
   for (int c = 0; c < kNumClasses; ++c)
-    for (int k = threadIdx.x; k <= ncta_eff[c]; k += kPlanThreads)
+    for (int k = threadIdx.x; k <= ncta_eff[c]; k += blockDim.x)
       cta_start[c * (kMaxCtas + 1) + k] = s_start[c][k];
 
   // pass 2: per unit (b, h) — segments and partial rows
   const int num_units = num_seqs * num_kv_heads;
   int run_rows = 0;
-  for (int base = 0; base < num_units; base += kPlanThreads) {
+  for (int base = 0; base < num_units; base += (int)blockDim.x) {
     const int u = base + threadIdx.x;
     int rows = 0;
     if (u < num_units) {
@@ -462,7 +480,8 @@ cudaError_t launch_plan(const int32_t* context_lens, const int32_t* block_lens, 
                         int num_q_tokens, int window, unsigned char* ws, int* device_status,
                         cudaStream_t stream) {
   const size_t dyn = num_seqs <= kPlanSmemSeqs ? sizeof(PlanSmem) : 0;
-  plan_kernel<<<1, kPlanThreads, dyn, stream>>>(context_lens, block_lens, num_seqs, num_kv_heads,
+  const int threads = num_seqs <= kPlanSmallSeqs ? kPlanThreadsSmall : kPlanThreadsLarge;
+  plan_kernel<<<1, threads, dyn, stream>>>(context_lens, block_lens, num_seqs, num_kv_heads,
                                               group, max_pages, max_block_len, tile_tc, tile_simt,
                                               ncta_tc, ncta_simt, path, rows_bound, num_q_tokens,
                                               window, ws, device_status);

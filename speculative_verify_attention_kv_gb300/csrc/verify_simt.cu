@@ -242,8 +242,7 @@ cudaError_t launch_verify_simt(const AttnParams& p, int rows_cap, int ncta, cuda
   const size_t smem = simt_smem_bytes(p.head_dim, rows_cap);
 #define SPLASH_SIMT(DD)                                                                        \
   do {                                                                                         \
-    cudaError_t e = cudaFuncSetAttribute(verify_simt_kernel<DD>,                               \
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); \
+    cudaError_t e = ensure_dynamic_smem<verify_simt_kernel<DD>>((int)smem);                   \
     if (e != cudaSuccess) return e;                                                            \
     e = launch_dependent(verify_simt_kernel<DD>, dim3(ncta), dim3(kSimtThreads), smem, stream, \
                          p, rows_cap);                                                         \

@@ -16,17 +16,20 @@
 // folded into P before P is rounded to fp16.
 //
 // Warp roles (512 threads):
-//   warps 0-7   softmax + epilogue: warp w owns TMEM lanes (rows) 32(w%4) +
-//               16(w/4) .. +15; with the 16x256b load shape each row is spread
-//               over 4 threads (2 rows per thread, row reductions = 2 shuffles)
+//   warps 0-7   softmax + epilogue: warp w owns TMEM lanes 32(w%4) + 16(w/4)
+//               .. +15; with the 16x256b load shape each lane's row is spread
+//               over 4 threads (2 rows per thread, row reductions = 2
+//               shuffles). A unit's R rows are spread evenly over the four
+//               lane quarters (row q*ceil(R/4) + i in lane 32q + i), so each
+//               SM sub-partition's softmax warps carry a quarter of them.
 //   warps 8-11  converters: int8 codes from the staging ring -> fp16 in
 //               registers -> 128B-swizzled SMEM tiles (K: K-major, V: MN-major)
 //   warp  12    TMEM allocation; one thread issues the QK MMAs of even tiles
 //   warp  13    one thread issues the QK MMAs of odd tiles
 //   warp  14    one thread issues the PV MMAs
-//               (one thread issues at most one tcgen05.mma per ~120 cycles
-//               whatever N is; with A in TMEM, three issuing threads give
-//               nearly three times the rate of one)
+//               (one thread issues a tcgen05.mma about every 45 cycles at
+//               N <= 128, while an N = 64 MMA needs 32 cycles of the tensor
+//               pipe: the QK issue is split over two threads)
 //   warp  15    producer: one bulk async copy (TMA, untiled) per (page, KV
 //               head) block, K and V codes together (8 KB at D = 256; the
 //               pool keeps them adjacent because a copy's issue cost is
@@ -37,12 +40,19 @@
 // QK of the tile is done), fp16 V tiles x2 (free once PV is done), scales x3.
 // A third staging stage bought with a V tile measured 5% faster: the copies'
 // latency, not the PV chain, limited the loop.
-// Handshakes are mbarriers; every wait gives up after ~1 s, sets
-// SPLASH_DEVICE_TIMEOUT and lets the CTA drain and free its TMEM.
-#include "splash_common.cuh"
+// Handshakes are mbarriers, one arrival per warp, with warp-uniform wait
+// results. Every wait gives up after AttnParams::wait_ns (1 s by default),
+// sets SPLASH_DEVICE_TIMEOUT and an abort flag; the CTA then lets the copies
+// and MMAs it issued complete and frees its TMEM.
+// The CTA's share of the tile stream (a contiguous range, cut by estimated
+// cost) and the units' segment layout come from the split planner; barriers
+// and TMEM are set up before the kernel waits for the plan (programmatic
+// dependent launch).
+#include "tcgen05_ptx.cuh"
 
 namespace splash {
 namespace tc {
+using namespace dev;
 
 constexpr int kTileKeys = 64;
 constexpr int kPagesPerTile = kTileKeys / kPageSize;
@@ -63,9 +73,6 @@ static_assert(kThreads == 512, "warp roles");
 static_assert(kStages == 2, "one QK-issuing warp per S/P buffer");
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.0f;          // lazy rescale threshold (factor 256)
-// limit of the drain waits (copies and MMAs already issued land before the
-// CTA frees its TMEM and exits); the pipeline waits use AttnParams::wait_ns
-constexpr unsigned long long kDrainNs = 1000000000ull;
 
 template <int D>
 struct Cfg {
@@ -91,210 +98,6 @@ struct Cfg {
   static constexpr int kSmemBytes = kSmemAligned > 120 * 1024 ? kSmemAligned : 120 * 1024;
   static_assert(kSmemUsed <= kSmemMax, "shared memory budget");
 };
-
-// ---------------------------------------------------------------- PTX helpers
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ unsigned long long global_ns() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.b32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// One arrival per warp: every lane's prior writes (and tcgen05 / proxy fences)
-// are ordered before lane 0's release by the warp barrier.
-__device__ __forceinline__ void warp_arrive(uint32_t bar, int lane) {
-  __syncwarp();
-  if (lane == 0) mbar_arrive(bar);
-}
-
-__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.b32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-struct Sync {
-  volatile int* abort_flag;
-  int* status;
-  unsigned long long limit_ns;
-  // Bounded wait for the phase of `parity` to complete. false = gave up.
-  __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity) const {
-    if (mbar_try_wait(bar, parity)) return true;
-    const unsigned long long t0 = global_ns();
-    while (true) {
-      if (mbar_try_wait(bar, parity)) return true;
-      if (*abort_flag) return false;
-      if (global_ns() - t0 > limit_ns) {
-        *abort_flag = 1;
-        report(status, SPLASH_DEVICE_TIMEOUT);
-        return false;
-      }
-    }
-  }
-  // Bounded wait that ignores the abort flag: lets copies already in flight
-  // land before the CTA exits. false = gave up.
-  __device__ __forceinline__ bool drain(uint32_t bar, uint32_t parity) const {
-    const unsigned long long t0 = global_ns();
-    while (!mbar_try_wait(bar, parity))
-      if (global_ns() - t0 > kDrainNs) return false;
-    return true;
-  }
-};
-
-__device__ __forceinline__ float fmax3(float a, float b, float c) {
-  float y;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(y) : "f"(a), "f"(b), "f"(c));
-  return y;
-}
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-__device__ __forceinline__ void fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void fence_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-// smem matrix descriptor, 128-byte swizzle (sm_100 encoding, version 1)
-__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-  uint64_t d = 0;
-  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
-  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
-  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
-  d |= (uint64_t)1 << 46;
-  d |= (uint64_t)2 << 61;
-  return d;
-}
-// instruction descriptor: kind::f16, fp16 A and B, fp32 D, A K-major
-__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, int b_mn_major) {
-  return (1u << 4) | (0u << 7) | (0u << 10) | (0u << 15) | ((uint32_t)b_mn_major << 16) |
-         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
-}
-
-__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                       uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
-      ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-      : "memory");
-}
-
-#define SPLASH_R8(i) "=r"(v[i]), "=r"(v[i + 1]), "=r"(v[i + 2]), "=r"(v[i + 3]), \
-                     "=r"(v[i + 4]), "=r"(v[i + 5]), "=r"(v[i + 6]), "=r"(v[i + 7])
-#define SPLASH_W8(i) "r"(v[i]), "r"(v[i + 1]), "r"(v[i + 2]), "r"(v[i + 3]), \
-                     "r"(v[i + 4]), "r"(v[i + 5]), "r"(v[i + 6]), "r"(v[i + 7])
-
-// 32 consecutive columns of this thread's lane
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
-      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
-      "%28, %29, %30, %31}, [%32];"
-      : SPLASH_R8(0), SPLASH_R8(8), SPLASH_R8(16), SPLASH_R8(24)
-      : "r"(taddr));
-}
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
-      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
-      "%28, %29, %30, %31, %32};"
-      ::"r"(taddr), SPLASH_W8(0), SPLASH_W8(8), SPLASH_W8(16), SPLASH_W8(24)
-      : "memory");
-}
-// 16 lanes x 64 columns (16x256b, 8 repetitions): thread t holds, for
-// repetition i, columns 8i + 2(t%4) + {0,1} of lane base + t/4 (v[4i], v[4i+1])
-// and of lane base + 8 + t/4 (v[4i+2], v[4i+3])
-__device__ __forceinline__ void tmem_ld16x256_x8(uint32_t taddr, uint32_t (&v)[32]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.16x256b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
-      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
-      "%28, %29, %30, %31}, [%32];"
-      : SPLASH_R8(0), SPLASH_R8(8), SPLASH_R8(16), SPLASH_R8(24)
-      : "r"(taddr));
-}
-__device__ __forceinline__ void tmem_st16x256_x8(uint32_t taddr, const uint32_t (&v)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.16x256b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
-      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
-      "%28, %29, %30, %31, %32};"
-      ::"r"(taddr), SPLASH_W8(0), SPLASH_W8(8), SPLASH_W8(16), SPLASH_W8(24)
-      : "memory");
-}
-// 16 lanes x 64 columns (16x128b, 16 repetitions): repetition i holds column
-// 4i + t%4 of lane base + t/4 (v[2i]) and of lane base + 8 + t/4 (v[2i+1])
-__device__ __forceinline__ void tmem_st16x128_x16(uint32_t taddr, const uint32_t (&v)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.16x128b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
-      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
-      "%28, %29, %30, %31, %32};"
-      ::"r"(taddr), SPLASH_W8(0), SPLASH_W8(8), SPLASH_W8(16), SPLASH_W8(24)
-      : "memory");
-}
-// 16 lanes x 32 columns (16x128b, 8 repetitions), same layout as above
-__device__ __forceinline__ void tmem_st16x128_x8(uint32_t taddr, const uint32_t (&v)[16]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.16x128b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
-      "%11, %12, %13, %14, %15, %16};"
-      ::"r"(taddr), SPLASH_W8(0), SPLASH_W8(8)
-      : "memory");
-}
-__device__ __forceinline__ void tmem_wait_ld() {
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_wait_st() {
-  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-
-// 4 int8 codes -> 2 x half2 (exact): 1024 + (c + 128) built by byte permute, minus 1152
-__device__ __forceinline__ void i8x4_to_h2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
-  const uint32_t u = w ^ 0x80808080u;
-  uint32_t a, b;
-  asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(a) : "r"(u), "r"(0x64646464u));
-  asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(b) : "r"(u), "r"(0x64646464u));
-  const __half2 bias = __floats2half2_rn(1152.f, 1152.f);
-  __half2 ha = __hsub2(*reinterpret_cast<__half2*>(&a), bias);
-  __half2 hb = __hsub2(*reinterpret_cast<__half2*>(&b), bias);
-  lo = *reinterpret_cast<uint32_t*>(&ha);
-  hi = *reinterpret_cast<uint32_t*>(&hb);
-}
 
 // ------------------------------------------------------------- work iteration
 struct Seg {
@@ -349,17 +152,6 @@ struct Smem {
   int abort_flag;
 };
 
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
-                                         uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-      ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
-      : "memory");
-}
 
 // Page ids of a sequence, 32 at a time: lane l holds entry base + l of the
 // sequence's page-table row (-1 past the pages the sequence needs). The next
@@ -697,7 +489,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
             ks2[2 * i4] = make_float2(kq.x, kq.y);
             ks2[2 * i4 + 1] = make_float2(kq.z, kq.w);
           }
-          tmem_wait_ld();
+          tmem_wait_ld(sv);         // sv is read only after the wait
           // x = S * sK (packed fp32x2); masked columns -> -inf (their scales
           // are not read: pages past the end may hold anything)
           // this thread's keys: 16*quad + 2i + {0,1} (see tile_row_of_key)
@@ -799,7 +591,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
           for (int c0 = 0; c0 < D; c0 += 64) {
             uint32_t v[32];
             tmem_ld16x256_x8(tmem + lane_base + C::kOCol + c0, v);
-            tmem_wait_ld();
+            tmem_wait_ld(v);
 #pragma unroll
             for (int i = 0; i < 8; ++i)
 #pragma unroll
@@ -842,7 +634,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
         for (int c0 = 0; c0 < D; c0 += 64) {
           uint32_t v[32];
           tmem_ld16x256_x8(tmem + lane_base + C::kOCol + c0, v);
-          tmem_wait_ld();
+          tmem_wait_ld(v);
 #pragma unroll
           for (int k = 0; k < 2; ++k) {
             if (!live[k]) continue;
@@ -952,8 +744,8 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
     const int qk_par = warp - kMmaWarp;          // tiles of this parity (QK issuers)
     const int role = is_qk ? qk_par : 2;
     if (lane == 0) {
-      constexpr uint32_t kIdescQK = idesc_f16(128, kTileKeys, 0);
-      constexpr uint32_t kIdescPV = idesc_f16(128, D, 1);
+      constexpr uint32_t kIdescQK = idesc_f16(128, kTileKeys, 0, 0);
+      constexpr uint32_t kIdescPV = idesc_f16(128, D, 0, 1);
       // descriptors of k-step 0 of buffer 0; buffers and k-steps add byte offsets >> 4
       const uint64_t kdesc0 = sdesc(smem_u32(kbuf), 16, 1024);
       const uint64_t vdesc0 = sdesc(smem_u32(vbuf), kTileKeys * 128, 1024);
@@ -1026,8 +818,7 @@ cudaError_t launch_verify_tc(const AttnParams& p, int rows_cap, int ncta, cudaSt
 #define SPLASH_TC(DD, SWA)                                                                     \
   do {                                                                                         \
     constexpr int smem = tc::Cfg<DD>::kSmemBytes;                                              \
-    cudaError_t e = cudaFuncSetAttribute(tc::verify_tc_kernel<DD, SWA>,                        \
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);   \
+    cudaError_t e = ensure_dynamic_smem<tc::verify_tc_kernel<DD, SWA>>(smem);                 \
     if (e != cudaSuccess) return e;                                                            \
     e = launch_dependent(tc::verify_tc_kernel<DD, SWA>, dim3(ncta), dim3(tc::kThreads), smem,  \
                          stream, p);                                                           \

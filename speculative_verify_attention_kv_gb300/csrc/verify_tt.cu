@@ -977,15 +977,13 @@ cudaError_t launch_verify_tt(const AttnParams& p, const CUtensorMap& map, int nc
   constexpr int smem = tt::kSmemBytes;
   cudaError_t e;
   if (p.window > 0) {
-    e = cudaFuncSetAttribute(tt::verify_tt_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smem);
+    e = ensure_dynamic_smem<tt::verify_tt_kernel<true>>(smem);
     if (e != cudaSuccess) return e;
     e = launch_dependent(tt::verify_tt_kernel<true>, dim3(ncta), dim3(tt::kThreads), smem, stream, p,
                          map);
     if (e != cudaSuccess) return e;
   } else {
-    e = cudaFuncSetAttribute(tt::verify_tt_kernel<false>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    e = ensure_dynamic_smem<tt::verify_tt_kernel<false>>(smem);
     if (e != cudaSuccess) return e;
     e = launch_dependent(tt::verify_tt_kernel<false>, dim3(ncta), dim3(tt::kThreads), smem, stream, p,
                          map);

@@ -184,6 +184,10 @@ SMALL = [
     dict(hq=32, hkv=4, D=128, ctx=[333], T=[16]),          # T*G = 128 rows
     dict(hq=24, hkv=4, D=256, ctx=[50, 60, 70], T=[3, 0, 2]),   # an idle sequence
     dict(hq=24, hkv=4, D=256, ctx=[4000], T=[4]),
+    # more sequences than the small planner block takes (the 1024-thread planner)
+    dict(hq=8, hkv=2, D=128,
+         ctx=[int(x) for x in np.random.default_rng(71).integers(0, 300, 200)],
+         T=[int(x) for x in np.random.default_rng(72).integers(0, 5, 200)]),
 ]
 
 
