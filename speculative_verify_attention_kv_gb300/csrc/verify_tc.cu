@@ -734,8 +734,9 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
           // the codes of the tile kRing ahead into L2 only (no shared
           // memory): its staging copy, issued when this ring stage frees
           // again, then hits L2. Measured 5-6% faster on 16 x 32K and the
-          // ragged batch; 2 to 4 tiles ahead do the same, 6 less, and
-          // prefetching the 64-byte scale rows as well is slower.
+          // ragged batch; 2 to 4 tiles ahead do the same, 6 less. The scale
+          // rows take plain L2 prefetches (bulk prefetches of 64 bytes each
+          // measured slower).
           const int ahead = it + kRing;
           const int k0a = ahead * kTileKeys;
           const int pg = win.peek(s.b, k0a / kPageSize + (lane & 3));
@@ -744,6 +745,14 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
             asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;"
                          ::"l"(p.k_pages + code_offset(pg, s.h, p.num_kv_heads, 0, D)),
                          "r"((uint32_t)(2 * kPageSize * D)) : "memory");
+          // and its K / V scale rows (64 bytes each) with plain L2 prefetches
+          const int pgs = __shfl_sync(0xffffffffu, pg, lane & 3);
+          if (ahead < s.i1 && lane >= 4 && lane < 12 && k0a + kPageSize * (lane & 3) < s.Lk &&
+              pgs >= 0 && pgs < p.num_pages) {
+            const size_t sc = ((size_t)pgs * p.num_kv_heads + s.h) * kPageSize;
+            const float* src = (lane < 8 ? p.k_scales : p.v_scales) + sc;
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(src) : "memory");
+          }
         }
       }
     }
