@@ -740,15 +740,17 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
           const int ahead = it + kRing;
           const int k0a = ahead * kTileKeys;
           const int pg = win.peek(s.b, k0a / kPageSize + (lane & 3));
-          if (ahead < s.i1 && lane < kPagesPerTile && k0a + kPageSize * (lane & 3) < s.Lk && pg >= 0 &&
-              pg < p.num_pages)
+          // the pages stage_codes will copy: inside the sequence and not
+          // wholly below a sliding window
+          const bool want = ahead < s.i1 && k0a + kPageSize * (lane & 3) < s.Lk &&
+                            k0a + kPageSize * ((lane & 3) + 1) > s.klo;
+          if (want && lane < kPagesPerTile && pg >= 0 && pg < p.num_pages)
             asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;"
                          ::"l"(p.k_pages + code_offset(pg, s.h, p.num_kv_heads, 0, D)),
                          "r"((uint32_t)(2 * kPageSize * D)) : "memory");
           // and its K / V scale rows (64 bytes each) with plain L2 prefetches
           const int pgs = __shfl_sync(0xffffffffu, pg, lane & 3);
-          if (ahead < s.i1 && lane >= 4 && lane < 12 && k0a + kPageSize * (lane & 3) < s.Lk &&
-              pgs >= 0 && pgs < p.num_pages) {
+          if (want && lane >= 4 && lane < 12 && pgs >= 0 && pgs < p.num_pages) {
             const size_t sc = ((size_t)pgs * p.num_kv_heads + s.h) * kPageSize;
             const float* src = (lane < 8 ? p.k_scales : p.v_scales) + sc;
             asm volatile("prefetch.global.L2 [%0];" ::"l"(src) : "memory");
