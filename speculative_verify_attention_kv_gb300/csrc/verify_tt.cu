@@ -120,7 +120,7 @@ struct Red {                    // softmax scratch
   float wmax[8];                // per softmax warp: max |q|
   volatile int slow_tile[2];    // by tile parity: the tile whose check failed. Two
                                 // slots: a warp may vote on tile g + 1 before a
-                                // slower one has read the verdict on tile g
+                                // slower one has read the decision for tile g
 };
 static_assert(sizeof(Red) <= kRedBytes, "scratch");
 
