@@ -513,15 +513,21 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
                             : make_float2(-INFINITY, -INFINITY);
           }
           // tile keys jj with nlo <= jj < nvis are visible to the row
-          int nvis[2], nlo[2];
+          int nvis[2] = {kTileKeys, kTileKeys}, nlo[2] = {-1, -1};
           bool full = true;
+          // a tile below the block's keys (and, with a window, above every
+          // row's lower bound) is visible to every row: no per-row bounds
+          const bool tile_inside = k0 + kTileKeys <= s.ctx &&
+                                   (!kSwa || s.ctx + s.T - window <= k0);
+          if (!tile_inside) {
 #pragma unroll
-          for (int k = 0; k < 2; ++k) {
-            nvis[k] = live[k] ? min(kTileKeys, lim[k] - k0 + 1) : 0;
-            nlo[k] = kSwa ? max(lo[k] - k0, -1) : -1;         // compile-time -1 without a window
-            // rows that hold no query row need no mask (their P only reaches
-            // output rows that are never read)
-            full = full && (!live[k] || (nvis[k] == kTileKeys && (!kSwa || nlo[k] <= 0)));
+            for (int k = 0; k < 2; ++k) {
+              nvis[k] = live[k] ? min(kTileKeys, lim[k] - k0 + 1) : 0;
+              nlo[k] = kSwa ? max(lo[k] - k0, -1) : -1;       // compile-time -1 without a window
+              // rows that hold no query row need no mask (their P only reaches
+              // output rows that are never read)
+              full = full && (!live[k] || (nvis[k] == kTileKeys && (!kSwa || nlo[k] <= 0)));
+            }
           }
           if (!full) {
 #pragma unroll
@@ -534,14 +540,23 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
               }
           }
           float base[2] = {0.f, 0.f};
+          // both row sets' maxima at once (independent chains); the second is
+          // unused when the warp's second row set holds no row
+          float mts[2];
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            mts[k] = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) mts[k] = fmax3(mts[k], x[k][i].x, x[k][i].y);
+          }
+#pragma unroll
+          for (int k = 0; k < 2; ++k) mts[k] = fmaxf(mts[k], __shfl_xor_sync(0xffffffffu, mts[k], 1));
+#pragma unroll
+          for (int k = 0; k < 2; ++k) mts[k] = fmaxf(mts[k], __shfl_xor_sync(0xffffffffu, mts[k], 2));
 #pragma unroll
           for (int k = 0; k < 2; ++k) {
             if (k == 1 && !k1_live) break;                // no row in the warp's second set
-            float mt = -INFINITY;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) mt = fmax3(mt, x[k][i].x, x[k][i].y);
-            mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 1));
-            mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 2));
+            const float mt = mts[k];
             const float m_new = fmaxf(m[k], mt);
             float m_use = m[k];
             if (m[k] == -INFINITY) {
