@@ -4,7 +4,9 @@
 One step = one pass of the whole hot path over the workload's batch:
 ``splash_kv_append`` of every sequence's verify block (quantise + scatter),
 then ``splash_verify_attention`` (split planner, attention kernel, log-sum-exp
-combine). Default workload: 16 sequences x 32768 cached tokens, 24 query / 4
+combine); sequences that share a prefix go through
+``splash_verify_attention_shared`` (the prefix read once per block of stacked
+query rows). Default workload: 16 sequences x 32768 cached tokens, 24 query / 4
 KV heads, head_dim 256, T = 16, int8 KV with 1% outlier channels.
 
 Timing: W warm-up steps, then the GPU is kept busy for at least 2 s of steps
@@ -59,6 +61,9 @@ def parse_args(argv=None):
     ap.add_argument("--path", type=int, default=0,
                     help="0 auto, 1 CUDA-core, 2 tensor-core, 3 transposed tensor-core")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-stack", action="store_true",
+                    help="sequences that share a prefix go through splash_verify_attention "
+                         "(each reads the prefix itself) instead of the shared-prefix entry point")
     ap.add_argument("--eager", action="store_true",
                     help="call the library every step instead of replaying captured graphs")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
@@ -352,9 +357,7 @@ def run_ours(args):
         ev = (ev_kb[timed_k], ev_ka[timed_k]) if kernel_events else None
         if timed_k is not None and not kernel_events:
             ev_b[timed_k].record(stream)
-        sk.splash_verify_attention(dw.q, *dw.pool, dw.table, dw.ctx, dw.T, float(W.sm_scale),
-                                   dw.max_T, dw.out, dw.lse, dw.ws, device_status=dw.status,
-                                   path=args.path, events=ev)
+        dw.attend(path=args.path, events=ev, stack=not args.no_stack)
         if timed_k is not None and not kernel_events:
             ev_c[timed_k].record(stream)
 
@@ -379,9 +382,7 @@ def run_ours(args):
                 with torch.cuda.graph(g_app):
                     dw.append_block()
                 with torch.cuda.graph(g_att):
-                    sk.splash_verify_attention(dw.q, *dw.pool, dw.table, dw.ctx, dw.T,
-                                               float(W.sm_scale), dw.max_T, dw.out, dw.lse, dw.ws,
-                                               device_status=dw.status, path=args.path)
+                    dw.attend(path=args.path, stack=not args.no_stack)
                 caught.append((g_app, g_att))
             launches_per_step = (sk.splash_launch_count() - c0) // n_copies
             graphs = caught
@@ -445,9 +446,11 @@ def run_ours(args):
     h_v = dw.v_new.cpu().pin_memory()
     h_ctx = dw.ctx.cpu().pin_memory()
     h_T = dw.T.cpu().pin_memory()
+    h_sl = dw.shared_lens.cpu().pin_memory() if dw.shared_lens is not None else None
     h_out = torch.empty(dw.out.shape, dtype=dw.out.dtype).pin_memory()
     h_lse = torch.empty(dw.lse.shape, dtype=dw.lse.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_ctx, h_T))
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_ctx, h_T, h_sl)
+              if t is not None)
     d2h = sum(t.numel() * t.element_size() for t in (h_out, h_lse))
 
     def e2e_step(j):
@@ -456,9 +459,12 @@ def run_ours(args):
         dw.v_new.copy_(h_v, non_blocking=True)
         dw.ctx.copy_(h_ctx, non_blocking=True)
         dw.T.copy_(h_T, non_blocking=True)
+        if h_sl is not None:
+            dw.shared_lens.copy_(h_sl, non_blocking=True)
         dw.use_pool(j)
         if has_work:
-            dw.step()
+            dw.append_block()
+            dw.attend(path=args.path, stack=not args.no_stack)
         h_out.copy_(dw.out, non_blocking=True)
         h_lse.copy_(dw.lse, non_blocking=True)
 
@@ -504,6 +510,7 @@ def run_ours(args):
                    "head_dim": W_full.spec.head_dim, "page": W_full.spec.page_size,
                    "verify_tokens_per_step": n_tok, "algorithmic_bytes": algo_full,
                    "l2": l2_note, "path": args.path, "launch": launch_mode,
+                   "prefix_stacking": bool(W.prefix_len) and not args.no_stack,
                    "t_attn_ms": t_attn_max, "attention_kernel_ms": attn_max,
                    "hbm_gbs": achieved, "hbm_frac": achieved / peak,
                    "parallelism": (f"{world} ranks, sequences partitioned by KV bytes"

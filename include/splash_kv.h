@@ -289,6 +289,72 @@ int splash_verify_attention_profiled(const uint16_t* q, int num_q_tokens,
                                      struct CUevent_st* attn_begin, struct CUevent_st* attn_end);
 
 /*
+ * splash_verify_attention_shared — splash_verify_attention for a batch whose
+ * sequences share prefix pages, reading each shared prefix tile once for the
+ * stacked query rows of all sequences that share it.
+ *
+ * The Splash article on discuss.pytorch.kr indexes the paged KV cache by
+ * prefix, so requests with a common prefix point at the same pages (section
+ * "배치 스케줄링과 시작 시점에 확정되는 메모리 예산"), and it measures
+ * concurrent agent requests that share a long prefix (section "동시 요청에서 더
+ * 벌어지는 격차"). This entry point extends the reuse of one KV tile across the
+ * query rows of a sequence to the rows of every sequence sharing the tile.
+ *
+ *   shared_lens: int32 [num_seqs] (device, non-NULL). shared_lens[b] > 0 states
+ *     that logical keys 0 .. shared_lens[b] - 1 of sequence b sit in the same
+ *     pages as those of sequence b - 1 (equal page-table entries); 0 states
+ *     nothing; shared_lens[0] is ignored. The caller guarantees the claim.
+ *     The library only clamps it to both sequences' context_lens: a claim
+ *     whose pages differ gives sequence b the keys of sequence b - 1's pages.
+ *
+ * A run of consecutive sequences b0 .. b1, each linked to the one before it
+ * by at least 64 keys, is a prefix group. Its common prefix is the smallest
+ * link, cut to every member's context and down to a multiple of 64 keys. The
+ * members' query rows (sum of T_b * G), stacked in sequence order, are cut
+ * into blocks of 128 rows. Each block reads the common prefix through the
+ * pages of b0's page-table row. Each member reads only its own keys after
+ * the prefix. The log-sum-exp combine then merges the two partial results of
+ * every row. A group is stacked only when it needs fewer blocks than it has
+ * members (e.g. four sequences of T * G = 96 rows: 3 blocks instead of 4
+ * passes over the prefix; four of 6 rows: 1 block).
+ *
+ * Output, result and error contract as splash_verify_attention. The result
+ * equals splash_verify_attention's within rounding, since the same scores are
+ * summed in a different split. Groups apply only on the tensor-core kernel
+ * (path 0 or 2, head_dim 128 or 256), and on batches of at most 1024
+ * sequences. Elsewhere the call computes the same result without stacking.
+ * The workspace must hold splash_verify_attention_shared_workspace_size bytes
+ * (more than splash_verify_attention's: every grouped row leaves two partial
+ * rows). shared_lens == NULL is SPLASH_ERR_INVALID_ARGUMENT.
+ */
+size_t splash_verify_attention_shared_workspace_size(int num_seqs, int num_q_tokens,
+                                                     int num_q_heads, int num_kv_heads,
+                                                     int head_dim, int max_block_len);
+int splash_verify_attention_shared(const uint16_t* q, int num_q_tokens,
+                                   const int8_t* k_pages, const int8_t* v_pages,
+                                   const float* k_scales, const float* v_scales,
+                                   const int32_t* page_table, int max_pages_per_seq,
+                                   const int32_t* context_lens, const int32_t* block_lens,
+                                   const int32_t* shared_lens, int num_seqs, int num_q_heads,
+                                   int num_kv_heads, int head_dim, int page_size, int num_pages,
+                                   int max_block_len, float sm_scale, uint16_t* out, float* lse,
+                                   void* workspace, size_t workspace_bytes, int* device_status,
+                                   struct CUstream_st* stream);
+/*
+ * splash_verify_attention_shared_profiled — splash_verify_attention_shared
+ * with path and ctas_per_class as in splash_verify_attention_tuned, and the
+ * two events of splash_verify_attention_profiled (either may be NULL).
+ */
+int splash_verify_attention_shared_profiled(
+    const uint16_t* q, int num_q_tokens, const int8_t* k_pages, const int8_t* v_pages,
+    const float* k_scales, const float* v_scales, const int32_t* page_table,
+    int max_pages_per_seq, const int32_t* context_lens, const int32_t* block_lens,
+    const int32_t* shared_lens, int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+    int page_size, int num_pages, int max_block_len, float sm_scale, uint16_t* out, float* lse,
+    void* workspace, size_t workspace_bytes, int* device_status, struct CUstream_st* stream,
+    int path, int ctas_per_class, struct CUevent_st* attn_begin, struct CUevent_st* attn_end);
+
+/*
  * splash_verify_attention_fixed_scratch — splash_verify_attention without a
  * caller-provided workspace, for callers that cannot allocate device memory:
  * for example code that runs under a memory manager owning every device

@@ -16,13 +16,13 @@ cudaError_t launch_kv_append_bf16(const __nv_bfloat16*, const __nv_bfloat16*, in
                                   const int32_t*, int, int, int, int, int*, cudaStream_t);
 cudaError_t launch_accept_commit(const int32_t*, const int32_t*, int, const int32_t*, int32_t*,
                                  int32_t*, int32_t*, int, int*, cudaStream_t);
-cudaError_t launch_plan(const int32_t*, const int32_t*, int, int, int, int, int, int, int, int,
-                        int, int, int, int, int, unsigned char*, int*, cudaStream_t);
-cudaError_t launch_combine(int, int, int, int, int, int, int, int, const unsigned char*,
+cudaError_t launch_plan(const int32_t*, const int32_t*, const int32_t*, int, int, int, int, int,
+                        int, int, int, int, int, int, int, int, unsigned char*, int*, cudaStream_t);
+cudaError_t launch_combine(int, int, int, int, int, int, int, int, bool, const unsigned char*,
                            __nv_bfloat16*, float*, cudaStream_t);
 cudaError_t launch_verify_simt(const AttnParams&, int, int, cudaStream_t);
 size_t simt_smem_bytes(int, int);
-cudaError_t launch_verify_tc(const AttnParams&, int, int, cudaStream_t);
+cudaError_t launch_verify_tc(const AttnParams&, int, int, bool, cudaStream_t);
 bool tc_supported(int head_dim);
 bool tt_supported(int head_dim, int rows_cap);
 int tt_tile_keys();
@@ -68,11 +68,17 @@ void default_ctas(int sms, int head_dim, int rows_cap, int* ncta_tc, int* ncta_s
   *ncta_simt = sms * per_sm < kMaxCtas ? sms * per_sm : kMaxCtas;
 }
 
+// Partial rows a plan can use. A CTA's tile range covers at most two units
+// that other CTAs share (its first and its last), so split units hold at most
+// 2 * (CTAs) segments of at most `rows` rows each. With prefix groups, row
+// blocks hold up to kMaxRows rows, and a grouped unit writes partials even
+// when one CTA covers it: every grouped output row then has one such row in
+// its block and one in its own unit.
 long long rows_bound_for(int num_q_tokens, int num_q_heads, int rows_cap, int ncta_tc,
-                         int ncta_simt) {
-  (void)num_q_tokens;
-  (void)num_q_heads;
-  return 2LL * rows_cap * ((long long)ncta_tc + ncta_simt) + 1;
+                         int ncta_simt, bool prefix_groups) {
+  if (!prefix_groups) return 2LL * rows_cap * ((long long)ncta_tc + ncta_simt) + 1;
+  const int rows = rows_cap > kMaxRows ? rows_cap : kMaxRows;
+  return 2LL * rows * ((long long)ncta_tc + ncta_simt) + 2LL * num_q_tokens * num_q_heads + 1;
 }
 
 }  // namespace
@@ -181,10 +187,11 @@ static int check_attn_shape(int num_q_tokens, int num_seqs, int num_q_heads, int
 
 static size_t workspace_bytes_for(int num_seqs, int num_q_tokens, int num_q_heads,
                                   int num_kv_heads, int head_dim, int max_block_len, int ncta_tc,
-                                  int ncta_simt) {
+                                  int ncta_simt, bool prefix_groups = false) {
   const int G = num_q_heads / num_kv_heads;
   const int rows_cap = max_block_len * G;
-  const long long rb = rows_bound_for(num_q_tokens, num_q_heads, rows_cap, ncta_tc, ncta_simt);
+  const long long rb =
+      rows_bound_for(num_q_tokens, num_q_heads, rows_cap, ncta_tc, ncta_simt, prefix_groups);
   return make_layout(num_seqs, num_kv_heads, head_dim, rb).total;
 }
 
@@ -200,6 +207,18 @@ size_t splash_verify_attention_workspace_size(int num_seqs, int num_q_tokens, in
                              max_block_len, sms, 4 * sms);
 }
 
+size_t splash_verify_attention_shared_workspace_size(int num_seqs, int num_q_tokens,
+                                                     int num_q_heads, int num_kv_heads,
+                                                     int head_dim, int max_block_len) {
+  if (check_attn_shape(num_q_tokens, num_seqs, num_q_heads, num_kv_heads, head_dim, kPageSize,
+                       max_block_len, 1) != SPLASH_OK)
+    return 0;
+  const int sms = device_sm_count();
+  if (sms <= 0) return 0;
+  return workspace_bytes_for(num_seqs, num_q_tokens, num_q_heads, num_kv_heads, head_dim,
+                             max_block_len, sms, 4 * sms, true);
+}
+
 }  // extern "C"
 
 // All attention entry points: window 0 is the full block-causal mask.
@@ -210,7 +229,8 @@ static int verify_impl(
     int num_q_heads, int num_kv_heads, int head_dim, int page_size, int num_pages,
     int max_block_len, float sm_scale, int window, uint16_t* out, float* lse, void* workspace,
     size_t workspace_bytes, int* device_status, struct CUstream_st* stream, int path,
-    int ctas_per_class, struct CUevent_st* attn_begin, struct CUevent_st* attn_end) {
+    int ctas_per_class, struct CUevent_st* attn_begin, struct CUevent_st* attn_end,
+    const int32_t* shared_lens = nullptr) {
   int st = check_attn_shape(num_q_tokens, num_seqs, num_q_heads, num_kv_heads, head_dim,
                             page_size, max_block_len, max_pages_per_seq);
   if (st != SPLASH_OK) return st;
@@ -254,16 +274,21 @@ static int verify_impl(
   int nt, ns;
   default_ctas(sms, head_dim, rows_simt > 0 ? rows_simt : 1, &nt, &ns);
   if (ctas_per_class > 0) nt = ns = ctas_per_class;
+  // prefix groups: the tensor-core kernel of 64-key tiles, without a window
+  // (elsewhere the same result is computed without them)
+  const bool groups = shared_lens != nullptr && window == 0 && path != 1 && tc_ok && !use_tt &&
+                      num_seqs <= kPrefixGroupMaxSeqs;
   const size_t need = workspace_bytes_for(num_seqs, num_q_tokens, num_q_heads, num_kv_heads,
-                                          head_dim, max_block_len, nt, ns);
+                                          head_dim, max_block_len, nt, ns, groups);
   if (workspace_bytes < need) return SPLASH_ERR_WORKSPACE_TOO_SMALL;
-  const long long rb = rows_bound_for(num_q_tokens, num_q_heads, rows_cap, nt, ns);
+  const long long rb = rows_bound_for(num_q_tokens, num_q_heads, rows_cap, nt, ns, groups);
   unsigned char* ws = static_cast<unsigned char*>(workspace);
   // in automatic mode, units too tall for the CUDA-core kernel's shared memory
   // go to the tensor-core kernel (the planner's row threshold already does so
   // for every unit with >= 16 rows).
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = counted(launch_plan(context_lens, block_lens, num_seqs, num_kv_heads, G,
+  cudaError_t e = counted(launch_plan(context_lens, block_lens, groups ? shared_lens : nullptr,
+                                      num_seqs, num_kv_heads, G,
                               max_pages_per_seq, max_block_len, use_tt ? tt_tile_keys() : kTcTile,
                               kSimtTile, nt, ns, path,
                               (int)rb, num_q_tokens, window, ws, device_status, s));
@@ -293,7 +318,7 @@ static int verify_impl(
   if (attn_begin && cudaEventRecord(reinterpret_cast<cudaEvent_t>(attn_begin), s) != cudaSuccess)
     return SPLASH_ERR_CUDA;
   if (path != 1 && tc_ok) {
-    e = counted(use_tt ? launch_verify_tt(p, tmap, nt, s) : launch_verify_tc(p, rows_cap, nt, s));
+    e = counted(use_tt ? launch_verify_tt(p, tmap, nt, s) : launch_verify_tc(p, rows_cap, nt, groups, s));
     if (e != cudaSuccess) return SPLASH_ERR_CUDA;
   }
   if (path != 2 && rows_simt > 0) {
@@ -303,7 +328,7 @@ static int verify_impl(
   if (attn_end && cudaEventRecord(reinterpret_cast<cudaEvent_t>(attn_end), s) != cudaSuccess)
     return SPLASH_ERR_CUDA;
   e = counted(launch_combine(num_q_tokens, num_q_heads, num_seqs, num_kv_heads, G, head_dim,
-                             (int)rb, sms, ws, p.out, lse, s));
+                             (int)rb, sms, groups, ws, p.out, lse, s));
   return e == cudaSuccess ? SPLASH_OK : SPLASH_ERR_CUDA;
 }
 
@@ -322,6 +347,39 @@ int splash_verify_attention_profiled(
                      num_kv_heads, head_dim, page_size, num_pages, max_block_len, sm_scale, 0, out,
                      lse, workspace, workspace_bytes, device_status, stream, path, ctas_per_class,
                      attn_begin, attn_end);
+}
+
+int splash_verify_attention_shared_profiled(
+    const uint16_t* q, int num_q_tokens, const int8_t* k_pages, const int8_t* v_pages,
+    const float* k_scales, const float* v_scales, const int32_t* page_table,
+    int max_pages_per_seq, const int32_t* context_lens, const int32_t* block_lens,
+    const int32_t* shared_lens, int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+    int page_size, int num_pages, int max_block_len, float sm_scale, uint16_t* out, float* lse,
+    void* workspace, size_t workspace_bytes, int* device_status, struct CUstream_st* stream,
+    int path, int ctas_per_class, struct CUevent_st* attn_begin, struct CUevent_st* attn_end) {
+  if (!shared_lens && num_seqs > 0 && num_q_tokens > 0) return SPLASH_ERR_INVALID_ARGUMENT;
+  return verify_impl(q, num_q_tokens, k_pages, v_pages, k_scales, v_scales, page_table,
+                     max_pages_per_seq, context_lens, block_lens, num_seqs, num_q_heads,
+                     num_kv_heads, head_dim, page_size, num_pages, max_block_len, sm_scale, 0, out,
+                     lse, workspace, workspace_bytes, device_status, stream, path, ctas_per_class,
+                     attn_begin, attn_end, shared_lens);
+}
+
+int splash_verify_attention_shared(const uint16_t* q, int num_q_tokens, const int8_t* k_pages,
+                                   const int8_t* v_pages, const float* k_scales,
+                                   const float* v_scales, const int32_t* page_table,
+                                   int max_pages_per_seq, const int32_t* context_lens,
+                                   const int32_t* block_lens, const int32_t* shared_lens,
+                                   int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                   int page_size, int num_pages, int max_block_len,
+                                   float sm_scale, uint16_t* out, float* lse, void* workspace,
+                                   size_t workspace_bytes, int* device_status,
+                                   struct CUstream_st* stream) {
+  return splash_verify_attention_shared_profiled(
+      q, num_q_tokens, k_pages, v_pages, k_scales, v_scales, page_table, max_pages_per_seq,
+      context_lens, block_lens, shared_lens, num_seqs, num_q_heads, num_kv_heads, head_dim,
+      page_size, num_pages, max_block_len, sm_scale, out, lse, workspace, workspace_bytes,
+      device_status, stream, 0, 0, nullptr, nullptr);
 }
 
 int splash_verify_attention_swa(const uint16_t* q, int num_q_tokens, const int8_t* k_pages,

@@ -49,6 +49,8 @@
 // cost) and the units' segment layout come from the split planner; barriers
 // and TMEM are set up before the kernel waits for the plan (programmatic
 // dependent launch).
+#include <type_traits>
+
 #include "tcgen05_ptx.cuh"
 
 namespace splash {
@@ -104,8 +106,13 @@ struct Cfg {
 struct Seg {
   int b, h, i0, i1, T, ctx, Lk, R, u;
   int klo;                        // first key any row of the unit sees
+  int qbase, r0;                  // items only: row r is query token qbase + (r0 + r) / G,
+                                  // head h * G + (r0 + r) % G
 };
 
+// The CTA's tiles [t, t_end) of the stream of all units, one segment (a run
+// of tiles of one unit) at a time. One item per sequence: units are
+// (sequence, KV head).
 struct SegIter {
   const int* stp;
   const int* seq_T;
@@ -131,6 +138,48 @@ struct SegIter {
     return true;
   }
 };
+
+// The same over the item table of a plan with prefix groups: units are
+// (item, KV head), and an item's rows and keys come from its descriptor.
+struct ItemSegIter {
+  const int* stp;                 // item prefix sums; entries past the items are INT_MAX
+  const ItemDesc* items;
+  int NB, G, Hkv;                 // NB: entries searched
+  int t, t_end;
+  __device__ bool next(Seg& s) {
+    if (t >= t_end) return false;
+    const int item = upper_index(stp, NB - 1, t);
+    const int4* dp = reinterpret_cast<const int4*>(items + item);
+    const int4 d0 = dp[0], d1 = dp[1];           // b, qbase, r0, R | ctx, Lk, klo, grouped
+    s.b = d0.x;
+    s.qbase = d0.y;
+    s.r0 = d0.z;
+    s.R = d0.w;
+    s.ctx = d1.x;
+    s.Lk = d1.y;
+    s.T = s.Lk - s.ctx;
+    s.klo = d1.z;
+    const int first = s.klo / kTileKeys;
+    const int tiles = (s.Lk + kTileKeys - 1) / kTileKeys - first;
+    const int local = t - stp[item];
+    s.h = local / tiles;
+    s.i0 = first + local % tiles;
+    s.i1 = min(first + tiles, s.i0 + (t_end - t));
+    s.u = item * Hkv + s.h;
+    t += s.i1 - s.i0;
+    return true;
+  }
+};
+
+template <bool kItems>
+__device__ __forceinline__ typename std::conditional<kItems, ItemSegIter, SegIter>::type
+make_iter(const int* stp, const int* seq_T, const int* seq_ctx, const ItemDesc* items, int B,
+          int G, int Hkv, int window, int t, int t_end) {
+  if constexpr (kItems)
+    return ItemSegIter{stp, items, max_items(B), G, Hkv, t, t_end};
+  else
+    return SegIter{stp, seq_T, seq_ctx, B, G, Hkv, window, t, t_end};
+}
 
 struct Smem {
   uint64_t ring_full[kRing];      // producer tx (K and V codes) -> converters
@@ -296,9 +345,11 @@ __device__ __forceinline__ void convert_codes(const uint8_t* src, uint8_t* dst, 
 
 // ------------------------------------------------------------------- kernel
 // kSwa: sliding-window instantiation (window read from the parameters); the
-// plain one compiles the window bounds out.
-template <int D, bool kSwa>
+// plain one compiles the window bounds out. kItems: the plan holds prefix
+// groups, and the kernel walks its item table (never with a window).
+template <int D, bool kSwa, bool kItems>
 __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
+  static_assert(!(kSwa && kItems), "prefix groups are planned without a window");
   using C = Cfg<D>;
   static_assert(sizeof(Smem) <= C::kBarBytes, "barrier area");
   extern __shared__ uint8_t smem_raw[];
@@ -369,7 +420,8 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
   const int* q_off = reinterpret_cast<const int*>(p.ws + L.q_off);
   const int* seq_T = reinterpret_cast<const int*>(p.ws + L.seq_T);
   const int* seq_ctx = reinterpret_cast<const int*>(p.ws + L.seq_ctx);
-  const int* stp = reinterpret_cast<const int*>(p.ws + L.stp) + kClassTensor * (B + 1);
+  const ItemDesc* items = reinterpret_cast<const ItemDesc*>(p.ws + L.items);
+  const int* stp = reinterpret_cast<const int*>(p.ws + L.stp0);
   const int* nseg = reinterpret_cast<const int*>(p.ws + L.nseg);
   const int* cfirst = reinterpret_cast<const int*>(p.ws + L.cfirst);
   const int* part_base = reinterpret_cast<const int*>(p.ws + L.part_base);
@@ -378,7 +430,9 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
 
   const int window = kSwa ? p.window : 0;
   const int* cst = reinterpret_cast<const int*>(p.ws + L.cta_start) + kClassTensor * (kMaxCtas + 1);
-  SegIter iter{stp, seq_T, seq_ctx, B, G, Hkv, window, cst[blockIdx.x], cst[blockIdx.x + 1]};
+  typename std::conditional<kItems, ItemSegIter, SegIter>::type iter =
+      make_iter<kItems>(stp, seq_T, seq_ctx, items, B, G, Hkv, window, cst[blockIdx.x],
+                        cst[blockIdx.x + 1]);
 
   if (warp < kSoftmaxWarps) {
     // ===================================================== softmax + epilogue
@@ -412,10 +466,18 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
         const int i = ln[k] & 31, r = (ln[k] >> 5) * rpq + i;
         live[k] = i < rpq && r < s.R;
         rr[k] = live[k] ? r : -1;
-        const int tt = live[k] ? r / G : 0, gg = live[k] ? r - tt * G : 0;
-        lim[k] = s.ctx + tt;                              // last visible key of the row
-        lo[k] = kSwa ? lim[k] - window + 1 : 0;           // first visible key (with a window)
-        qrow_off[k] = (size_t)(q_off[s.b] + tt) * p.num_q_heads + s.h * G + gg;
+        if constexpr (kItems) {
+          const int j = s.r0 + (live[k] ? r : 0);
+          const int tt = j / G, gg = j - tt * G;
+          lim[k] = s.ctx + tt;                            // last visible key of the row
+          lo[k] = 0;
+          qrow_off[k] = (size_t)(s.qbase + tt) * p.num_q_heads + s.h * G + gg;
+        } else {
+          const int tt = live[k] ? r / G : 0, gg = live[k] ? r - tt * G : 0;
+          lim[k] = s.ctx + tt;                            // last visible key of the row
+          lo[k] = kSwa ? lim[k] - window + 1 : 0;         // first visible key (with a window)
+          qrow_off[k] = (size_t)(q_off[s.b] + tt) * p.num_q_heads + s.h * G + gg;
+        }
       }
       const bool warp_live = __any_sync(0xffffffffu, live[0]);
       const bool k1_live = __any_sync(0xffffffffu, live[1]);   // second row set of the warp
@@ -643,7 +705,9 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
       if (!ok) break;
       fence_after();
       if (warp_live) {
-        const int ns = nseg[s.u];
+        // rows go to the output when one CTA covers the unit (and, with
+        // prefix groups, the unit is in none: part_base < 0 says both)
+        const int ns = kItems ? (part_base[s.u] < 0 ? 1 : 2) : nseg[s.u];
         float inv[2];
         long long prow[2];
 #pragma unroll
@@ -864,21 +928,31 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
 
 bool tc_supported(int head_dim) { return head_dim == 128 || head_dim == 256; }
 
-cudaError_t launch_verify_tc(const AttnParams& p, int rows_cap, int ncta, cudaStream_t stream) {
+cudaError_t launch_verify_tc(const AttnParams& p, int rows_cap, int ncta, bool items,
+                             cudaStream_t stream) {
   (void)rows_cap;
-#define SPLASH_TC(DD, SWA)                                                                     \
+#define SPLASH_TC(DD, SWA, IT)                                                                 \
   do {                                                                                         \
     constexpr int smem = tc::Cfg<DD>::kSmemBytes;                                              \
-    cudaError_t e = ensure_dynamic_smem<tc::verify_tc_kernel<DD, SWA>>(smem);                 \
+    cudaError_t e = ensure_dynamic_smem<tc::verify_tc_kernel<DD, SWA, IT>>(smem);             \
     if (e != cudaSuccess) return e;                                                            \
-    e = launch_dependent(tc::verify_tc_kernel<DD, SWA>, dim3(ncta), dim3(tc::kThreads), smem,  \
-                         stream, p);                                                           \
+    e = launch_dependent(tc::verify_tc_kernel<DD, SWA, IT>, dim3(ncta), dim3(tc::kThreads),    \
+                         smem, stream, p);                                                     \
     if (e != cudaSuccess) return e;                                                            \
   } while (0)
   const bool swa = p.window > 0;
+  if (swa && items) return cudaErrorInvalidValue;
   switch (p.head_dim) {
-    case 128: if (swa) SPLASH_TC(128, true); else SPLASH_TC(128, false); break;
-    case 256: if (swa) SPLASH_TC(256, true); else SPLASH_TC(256, false); break;
+    case 128:
+      if (swa) SPLASH_TC(128, true, false);
+      else if (items) SPLASH_TC(128, false, true);
+      else SPLASH_TC(128, false, false);
+      break;
+    case 256:
+      if (swa) SPLASH_TC(256, true, false);
+      else if (items) SPLASH_TC(256, false, true);
+      else SPLASH_TC(256, false, false);
+      break;
     default: return cudaErrorNotSupported;
   }
 #undef SPLASH_TC

@@ -44,8 +44,13 @@ class DeviceWorkload:
         self.out = torch.empty_like(self.q)
         self.lse = torch.empty(self.q.shape[:2], dtype=torch.float32, device=device)
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        # sequences that share a prefix go through the shared-prefix entry point
+        # (the prefix read once per row block of the stacked rows)
+        self.shared_lens = (torch.from_numpy(W.shared_lens()).to(device) if W.prefix_len
+                            else None)
         self.ws = sk.alloc_workspace(W.num_seqs, W.num_q_tokens, s.num_q_heads, s.num_kv_heads,
-                                     s.head_dim, self.max_T, device=device)
+                                     s.head_dim, self.max_T, device=device,
+                                     shared=self.shared_lens is not None)
         if populate:
             self.populate(seqs, chunk_tokens)
 
@@ -103,13 +108,20 @@ class DeviceWorkload:
                             device_status=self.status, stream=stream)
 
     def attend(self, path=sk.PATH_AUTO, ctas=0, out=None, lse=None, stream=None, window=0,
-               table=None):
+               table=None, stack=True, events=None, shared_lens=None):
+        """One verify-attention call. With a shared prefix (and no window) it
+        goes through the shared-prefix entry point unless ``stack`` is False;
+        ``shared_lens`` overrides the workload's own."""
         out = self.out if out is None else out
         lse = self.lse if lse is None else lse
+        sl = shared_lens if shared_lens is not None else self.shared_lens
+        if not stack or window != 0:
+            sl = None
         sk.splash_verify_attention(self.q, *self.pool, self.table if table is None else table,
                                    self.ctx, self.T, float(self.W.sm_scale), self.max_T, out, lse,
                                    self.ws, device_status=self.status, stream=stream, path=path,
-                                   ctas_per_class=ctas, window=window)
+                                   ctas_per_class=ctas, window=window, events=events,
+                                   shared_lens=sl)
         return out, lse
 
     def step(self, stream=None):

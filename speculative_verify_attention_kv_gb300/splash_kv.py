@@ -65,6 +65,14 @@ def _load() -> ctypes.CDLL:
     lib.splash_verify_attention_swa.argtypes = attn[:18] + [I] + attn[18:] + [I, I]
     lib.splash_verify_attention_profiled.restype = I
     lib.splash_verify_attention_profiled.argtypes = attn + [I, I, P, P]
+    lib.splash_verify_attention_shared_workspace_size.restype = S
+    lib.splash_verify_attention_shared_workspace_size.argtypes = [I, I, I, I, I, I]
+    # shared_lens follows block_lens
+    attn_sh = attn[:10] + [P] + attn[10:]
+    lib.splash_verify_attention_shared.restype = I
+    lib.splash_verify_attention_shared.argtypes = attn_sh
+    lib.splash_verify_attention_shared_profiled.restype = I
+    lib.splash_verify_attention_shared_profiled.argtypes = attn_sh + [I, I, P, P]
     lib.splash_verify_attention_fixed_scratch_bytes.restype = S
     lib.splash_verify_attention_fixed_scratch_bytes.argtypes = []
     lib.splash_verify_attention_fixed_scratch.restype = I
@@ -79,6 +87,8 @@ EXPORTED = ("splash_status_string", "splash_abi_version", "splash_tensor_path_su
             "splash_verify_attention_swa",
             "splash_verify_attention_workspace_size", "splash_verify_attention",
             "splash_verify_attention_tuned", "splash_verify_attention_profiled",
+            "splash_verify_attention_shared_workspace_size", "splash_verify_attention_shared",
+            "splash_verify_attention_shared_profiled",
             "splash_verify_attention_fixed_scratch_bytes", "splash_verify_attention_fixed_scratch")
 
 
@@ -206,24 +216,41 @@ def splash_verify_attention_workspace_size(num_seqs: int, num_q_tokens: int, num
         num_seqs, num_q_tokens, num_q_heads, num_kv_heads, head_dim, max_block_len))
 
 
+def splash_verify_attention_shared_workspace_size(num_seqs: int, num_q_tokens: int,
+                                                  num_q_heads: int, num_kv_heads: int,
+                                                  head_dim: int, max_block_len: int) -> int:
+    return int(LIB.splash_verify_attention_shared_workspace_size(
+        num_seqs, num_q_tokens, num_q_heads, num_kv_heads, head_dim, max_block_len))
+
+
 def alloc_workspace(num_seqs, num_q_tokens, num_q_heads, num_kv_heads, head_dim, max_block_len,
-                    device="cuda", ctas_per_class: int = 0) -> torch.Tensor:
-    n = splash_verify_attention_workspace_size(num_seqs, num_q_tokens, num_q_heads,
-                                               num_kv_heads, head_dim, max_block_len)
+                    device="cuda", ctas_per_class: int = 0, shared: bool = False) -> torch.Tensor:
+    """Workspace for splash_verify_attention (``shared``: for the shared-prefix
+    entry point)."""
+    query = (splash_verify_attention_shared_workspace_size if shared
+             else splash_verify_attention_workspace_size)
+    n = query(num_seqs, num_q_tokens, num_q_heads, num_kv_heads, head_dim, max_block_len)
     if n == 0:
         raise ValueError("invalid shape for the workspace size query")
     if ctas_per_class > 0:   # a fixed CTA count may need more partial rows than the default
-        n += 2 * max_block_len * (num_q_heads // num_kv_heads) * 2 * ctas_per_class * (head_dim + 1) * 4
+        rows = max_block_len * (num_q_heads // num_kv_heads)
+        if shared:
+            rows = max(rows, 128)
+        n += 2 * rows * 2 * ctas_per_class * (head_dim + 1) * 4
     return torch.empty(n, dtype=torch.uint8, device=device)
 
 
 def splash_verify_attention(q, k_pages, v_pages, k_scales, v_scales, page_table, context_lens,
                             block_lens, sm_scale: float, max_block_len: int, out, lse, workspace,
                             device_status=None, stream=None, path: int = PATH_AUTO,
-                            ctas_per_class: int = 0, events=None, window: int = 0) -> None:
+                            ctas_per_class: int = 0, events=None, window: int = 0,
+                            shared_lens=None) -> None:
     """``events``: optional (begin, end) torch.cuda.Event pair recorded around
     the attention kernels (the profiled entry point). ``window`` > 0: sliding
-    window of that many keys (splash_verify_attention_swa)."""
+    window of that many keys (splash_verify_attention_swa). ``shared_lens``:
+    int32 [num_seqs], keys each sequence shares with the one before it
+    (splash_verify_attention_shared; the workspace from
+    ``alloc_workspace(..., shared=True)``)."""
     _check(q, "q", torch.bfloat16, 3)
     _check(out, "out", torch.bfloat16, 3)
     _check(lse, "lse", torch.float32, 2)
@@ -245,7 +272,17 @@ def splash_verify_attention(q, k_pages, v_pages, k_scales, v_scales, page_table,
             context_lens.shape[0], hq, hkv, D, P, num_pages, int(max_block_len), float(sm_scale),
             _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(), _ptr(device_status),
             _stream(stream))
-    if window != 0:
+    if shared_lens is not None:
+        _check(shared_lens, "shared_lens", torch.int32, 1)
+        if shared_lens.shape[0] != context_lens.shape[0]:
+            raise ValueError("shared_lens must have one entry per sequence")
+        if window != 0:
+            raise ValueError("shared_lens is taken only without a window")
+        ev = [None, None] if events is None else [
+            ctypes.c_void_p(e.cuda_event) if e is not None else None for e in events]
+        st = LIB.splash_verify_attention_shared_profiled(*args[:10], _ptr(shared_lens), *args[10:],
+                                                         int(path), int(ctas_per_class), *ev)
+    elif window != 0:
         if events is not None:
             raise ValueError("events are recorded only without a window")
         st = LIB.splash_verify_attention_swa(*args[:18], int(window), *args[18:], int(path),

@@ -179,6 +179,14 @@ class Workload:
         sub.seq_ids = self.seq_ids[seqs]
         return sub
 
+    def shared_lens(self) -> np.ndarray:
+        """Keys each sequence shares (same pages) with the one before it:
+        int32 [num_seqs]; the shared prefix for every sequence but the first."""
+        out = np.zeros(self.num_seqs, dtype=np.int32)
+        if self.prefix_len and self.num_seqs > 1:
+            out[1:] = self.prefix_len
+        return out
+
     # ---- tensors --------------------------------------------------------
     def _apply_outliers(self, x: np.ndarray, h: int) -> np.ndarray:
         if self.outlier_channels is not None:

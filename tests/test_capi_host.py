@@ -144,3 +144,32 @@ def test_sliding_window_argument_errors(sk):
     args_bad_pool = list(args)
     args_bad_pool[3] = FAKE                                # V codes not at K + P*D
     assert f(*args_bad_pool, 5, *tail) == -1
+
+
+def _attn_shared(sk, **kw):
+    a = dict(q=FAKE, n=4, kp=FAKE, vp=FAKE_V, ks=FAKE, vs=FAKE, tab=FAKE, maxp=4, ctx=FAKE,
+             T=FAKE, sl=FAKE, B=1, hq=8, hkv=2, D=128, P=16, pages=8, maxT=4, sm=0.088, out=FAKE,
+             lse=FAKE, ws=FAKE, wsb=1 << 30, st=None, stream=None, path=0, ctas=0)
+    a.update(kw)
+    args = [a[k] for k in ("q", "n", "kp", "vp", "ks", "vs", "tab", "maxp", "ctx", "T", "sl", "B",
+                           "hq", "hkv", "D", "P", "pages", "maxT", "sm", "out", "lse", "ws", "wsb",
+                           "st", "stream")]
+    return sk.LIB.splash_verify_attention_shared_profiled(*args, a["path"], a["ctas"], None, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(sl=None), -1),              # the shared-prefix entry point needs shared_lens
+    (dict(hq=7), -1), (dict(D=100), -2), (dict(P=32), -2), (dict(maxT=40), -2),
+    (dict(path=4), -1), (dict(ctas=-1), -1), (dict(q=None), -1), (dict(ws=None), -1),
+    (dict(ws=ctypes.c_void_p(256 + 16)), -1), (dict(vp=FAKE), -1),
+    (dict(n=0), 0), (dict(B=0), 0), (dict(n=0, sl=None), 0),
+])
+def test_shared_prefix_argument_errors(sk, kw, code):
+    assert _attn_shared(sk, **kw) == code
+
+
+def test_shared_workspace_query_rejects_bad_shapes(sk):
+    f = sk.LIB.splash_verify_attention_shared_workspace_size
+    assert f(1, 4, 7, 2, 128, 4) == 0
+    assert f(1, 4, 8, 2, 100, 4) == 0
+    assert f(1, 4, 8, 2, 128, 64) == 0

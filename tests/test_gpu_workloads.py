@@ -94,13 +94,17 @@ def test_workload_every_sequence_matches_the_oracle(name):
     o_ref, l_ref = O.attention(q_values(W), opool, W.page_table, W.context_lens, W.block_lens,
                                s.num_kv_heads, float(W.sm_scale))
     rows_per_unit = int(W.block_lens.max()) * s.group
-    paths = [sk.PATH_AUTO]
+    # (path, stack): a shared prefix goes through the shared-prefix entry
+    # point (stacked rows) by default; it is also checked without stacking
+    runs = [(sk.PATH_AUTO, True)]
+    if W.prefix_len:
+        runs.append((sk.PATH_AUTO, False))
     if s.head_dim == 256 and rows_per_unit <= 96:
-        paths.append(sk.PATH_TENSOR_T)
-    for path in paths:
+        runs.append((sk.PATH_TENSOR_T, True))
+    for path, stack in runs:
         out = torch.full_like(dw.out, float("nan"))
         lse = torch.full_like(dw.lse, float("nan"))
-        dw.attend(path=path, out=out, lse=lse)
+        dw.attend(path=path, out=out, lse=lse, stack=stack)
         torch.cuda.synchronize()
         assert int(dw.status.item()) == 0
-        assert_parity(out, lse, o_ref, l_ref, what=f"{name} path {path}")
+        assert_parity(out, lse, o_ref, l_ref, what=f"{name} path {path} stack {stack}")
