@@ -6,6 +6,7 @@
 #include <cuda.h>
 
 #include "splash_common.cuh"
+#include "splash_groups.cuh"
 
 namespace splash {
 cudaError_t launch_kv_append(const float*, const float*, int, int8_t*, int8_t*, float*, float*,
@@ -16,13 +17,17 @@ cudaError_t launch_kv_append_bf16(const __nv_bfloat16*, const __nv_bfloat16*, in
                                   const int32_t*, int, int, int, int, int*, cudaStream_t);
 cudaError_t launch_accept_commit(const int32_t*, const int32_t*, int, const int32_t*, int32_t*,
                                  int32_t*, int32_t*, int, int*, cudaStream_t);
-cudaError_t launch_plan(const int32_t*, const int32_t*, const int32_t*, int, int, int, int, int,
-                        int, int, int, int, int, int, int, int, unsigned char*, int*, cudaStream_t);
-cudaError_t launch_combine(int, int, int, int, int, int, int, int, bool, const unsigned char*,
+cudaError_t launch_plan(const int32_t*, const int32_t*, int, int, int, int, int, int, int, int,
+                        int, int, int, int, int, unsigned char*, int*, cudaStream_t);
+cudaError_t launch_combine(int, int, int, int, int, int, int, int, const unsigned char*,
                            __nv_bfloat16*, float*, cudaStream_t);
 cudaError_t launch_verify_simt(const AttnParams&, int, int, cudaStream_t);
 size_t simt_smem_bytes(int, int);
 cudaError_t launch_verify_tc(const AttnParams&, int, int, bool, cudaStream_t);
+cudaError_t launch_plan_groups(const int32_t*, const int32_t*, const int32_t*, int, int, int, int,
+                               int, int, int, int, int, unsigned char*, int*, cudaStream_t);
+cudaError_t launch_combine_groups(int, int, int, int, int, int, int, int, const unsigned char*,
+                                  __nv_bfloat16*, float*, cudaStream_t);
 bool tc_supported(int head_dim);
 bool tt_supported(int head_dim, int rows_cap);
 int tt_tile_keys();
@@ -68,17 +73,11 @@ void default_ctas(int sms, int head_dim, int rows_cap, int* ncta_tc, int* ncta_s
   *ncta_simt = sms * per_sm < kMaxCtas ? sms * per_sm : kMaxCtas;
 }
 
-// Partial rows a plan can use. A CTA's tile range covers at most two units
-// that other CTAs share (its first and its last), so split units hold at most
-// 2 * (CTAs) segments of at most `rows` rows each. With prefix groups, row
-// blocks hold up to kMaxRows rows, and a grouped unit writes partials even
-// when one CTA covers it: every grouped output row then has one such row in
-// its block and one in its own unit.
 long long rows_bound_for(int num_q_tokens, int num_q_heads, int rows_cap, int ncta_tc,
-                         int ncta_simt, bool prefix_groups) {
-  if (!prefix_groups) return 2LL * rows_cap * ((long long)ncta_tc + ncta_simt) + 1;
-  const int rows = rows_cap > kMaxRows ? rows_cap : kMaxRows;
-  return 2LL * rows * ((long long)ncta_tc + ncta_simt) + 2LL * num_q_tokens * num_q_heads + 1;
+                         int ncta_simt) {
+  (void)num_q_tokens;
+  (void)num_q_heads;
+  return 2LL * rows_cap * ((long long)ncta_tc + ncta_simt) + 1;
 }
 
 }  // namespace
@@ -187,11 +186,10 @@ static int check_attn_shape(int num_q_tokens, int num_seqs, int num_q_heads, int
 
 static size_t workspace_bytes_for(int num_seqs, int num_q_tokens, int num_q_heads,
                                   int num_kv_heads, int head_dim, int max_block_len, int ncta_tc,
-                                  int ncta_simt, bool prefix_groups = false) {
+                                  int ncta_simt) {
   const int G = num_q_heads / num_kv_heads;
   const int rows_cap = max_block_len * G;
-  const long long rb =
-      rows_bound_for(num_q_tokens, num_q_heads, rows_cap, ncta_tc, ncta_simt, prefix_groups);
+  const long long rb = rows_bound_for(num_q_tokens, num_q_heads, rows_cap, ncta_tc, ncta_simt);
   return make_layout(num_seqs, num_kv_heads, head_dim, rb).total;
 }
 
@@ -215,8 +213,13 @@ size_t splash_verify_attention_shared_workspace_size(int num_seqs, int num_q_tok
     return 0;
   const int sms = device_sm_count();
   if (sms <= 0) return 0;
-  return workspace_bytes_for(num_seqs, num_q_tokens, num_q_heads, num_kv_heads, head_dim,
-                             max_block_len, sms, 4 * sms, true);
+  // without groups (a batch too large, a kernel without them) the plain plan runs
+  const size_t plain = workspace_bytes_for(num_seqs, num_q_tokens, num_q_heads, num_kv_heads,
+                                           head_dim, max_block_len, sms, 4 * sms);
+  const long long rb = group_rows_bound(num_q_tokens, num_q_heads,
+                                        max_block_len * (num_q_heads / num_kv_heads), sms);
+  const size_t grouped = make_group_layout(num_seqs, num_kv_heads, head_dim, rb).total;
+  return plain > grouped ? plain : grouped;
 }
 
 }  // extern "C"
@@ -274,24 +277,31 @@ static int verify_impl(
   int nt, ns;
   default_ctas(sms, head_dim, rows_simt > 0 ? rows_simt : 1, &nt, &ns);
   if (ctas_per_class > 0) nt = ns = ctas_per_class;
-  // prefix groups: the tensor-core kernel of 64-key tiles, without a window
-  // (elsewhere the same result is computed without them)
+  // prefix groups: on the tensor-core kernel of 64-key tiles, without a window,
+  // for batches of up to kPrefixGroupMaxSeqs (elsewhere the same result is
+  // computed without them)
   const bool groups = shared_lens != nullptr && window == 0 && path != 1 && tc_ok && !use_tt &&
                       num_seqs <= kPrefixGroupMaxSeqs;
-  const size_t need = workspace_bytes_for(num_seqs, num_q_tokens, num_q_heads, num_kv_heads,
-                                          head_dim, max_block_len, nt, ns, groups);
+  const long long rb = groups ? group_rows_bound(num_q_tokens, num_q_heads, rows_cap, nt)
+                              : rows_bound_for(num_q_tokens, num_q_heads, rows_cap, nt, ns);
+  const size_t need = groups ? make_group_layout(num_seqs, num_kv_heads, head_dim, rb).total
+                             : workspace_bytes_for(num_seqs, num_q_tokens, num_q_heads,
+                                                   num_kv_heads, head_dim, max_block_len, nt, ns);
   if (workspace_bytes < need) return SPLASH_ERR_WORKSPACE_TOO_SMALL;
-  const long long rb = rows_bound_for(num_q_tokens, num_q_heads, rows_cap, nt, ns, groups);
   unsigned char* ws = static_cast<unsigned char*>(workspace);
   // in automatic mode, units too tall for the CUDA-core kernel's shared memory
   // go to the tensor-core kernel (the planner's row threshold already does so
   // for every unit with >= 16 rows).
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = counted(launch_plan(context_lens, block_lens, groups ? shared_lens : nullptr,
-                                      num_seqs, num_kv_heads, G,
-                              max_pages_per_seq, max_block_len, use_tt ? tt_tile_keys() : kTcTile,
-                              kSimtTile, nt, ns, path,
-                              (int)rb, num_q_tokens, window, ws, device_status, s));
+  cudaError_t e =
+      groups ? counted(launch_plan_groups(context_lens, block_lens, shared_lens, num_seqs,
+                                          num_kv_heads, G, max_pages_per_seq, max_block_len,
+                                          kTcTile, nt, (int)rb, num_q_tokens, ws, device_status,
+                                          s))
+             : counted(launch_plan(context_lens, block_lens, num_seqs, num_kv_heads, G,
+                                   max_pages_per_seq, max_block_len,
+                                   use_tt ? tt_tile_keys() : kTcTile, kSimtTile, nt, ns, path,
+                                   (int)rb, num_q_tokens, window, ws, device_status, s));
   if (e != cudaSuccess) return SPLASH_ERR_CUDA;
 
   AttnParams p;
@@ -321,14 +331,16 @@ static int verify_impl(
     e = counted(use_tt ? launch_verify_tt(p, tmap, nt, s) : launch_verify_tc(p, rows_cap, nt, groups, s));
     if (e != cudaSuccess) return SPLASH_ERR_CUDA;
   }
-  if (path != 2 && rows_simt > 0) {
+  if (path != 2 && rows_simt > 0 && !groups) {
     e = counted(launch_verify_simt(p, rows_simt, ns, s));
     if (e != cudaSuccess) return SPLASH_ERR_CUDA;
   }
   if (attn_end && cudaEventRecord(reinterpret_cast<cudaEvent_t>(attn_end), s) != cudaSuccess)
     return SPLASH_ERR_CUDA;
-  e = counted(launch_combine(num_q_tokens, num_q_heads, num_seqs, num_kv_heads, G, head_dim,
-                             (int)rb, sms, groups, ws, p.out, lse, s));
+  e = groups ? counted(launch_combine_groups(num_q_tokens, num_q_heads, num_seqs, num_kv_heads, G,
+                                             head_dim, (int)rb, sms, ws, p.out, lse, s))
+             : counted(launch_combine(num_q_tokens, num_q_heads, num_seqs, num_kv_heads, G,
+                                      head_dim, (int)rb, sms, ws, p.out, lse, s));
   return e == cudaSuccess ? SPLASH_OK : SPLASH_ERR_CUDA;
 }
 

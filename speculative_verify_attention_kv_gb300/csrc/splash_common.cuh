@@ -23,9 +23,6 @@ constexpr int kMaxRows = 128;     // T*G limit per sequence and KV head
 // G = 6) it beats the CUDA-core kernel even at T*G = 6, so every unit goes
 // there when a tensor-core kernel exists for the head size.
 constexpr int kTensorMinRows = 1;
-// Prefix groups are planned for batches of up to this many sequences (the
-// planner keeps its per-sequence arrays in shared memory for them).
-constexpr int kPrefixGroupMaxSeqs = 1024;
 
 // Split of a class's tile stream over its CTAs by estimated cost, not by tile
 // count (a CTA's range is [cta_start[c], cta_start[c+1])). Cost of one tile of
@@ -50,8 +47,7 @@ struct PlanHeader {
   int total_part_rows;            // partial rows the split units use
   int rows_bound;                 // capacity of the partial buffers (rows)
   int window;                     // sliding window W (0: none)
-  int num_items;                  // tensor-core work items (>= num_seqs; see ItemDesc)
-  int pad_[3];
+  int pad_[4];
 };
 static_assert(sizeof(PlanHeader) == 64, "header size");
 
@@ -78,55 +74,17 @@ __host__ __device__ inline int unit_tiles(int ctx, int T, int window, int tile_k
   return (ctx + T + tile_keys - 1) / tile_keys - unit_first_tile(ctx, window, tile_keys);
 }
 
-// A work item of the tensor-core class: a set of query rows of one KV head
-// (the item's units are (item, KV head)) against a key range of one page-table
-// row. Item b < num_seqs is sequence b (its rows t * G + g, all its keys; with
-// a shared prefix, only the keys after it). Items past num_seqs are row blocks
-// of a prefix group: up to kMaxRows consecutive rows of the group's stacked
-// rows against the group's shared prefix keys.
-// Row r of an item is query token qbase + (r0 + r) / G, query head
-// h * G + (r0 + r) % G; it sees keys klo <= j < Lk with j <= ctx + (r0 + r) / G.
-struct ItemDesc {
-  int b;          // sequence whose page-table row holds the item's pages
-  int qbase;      // first query token of the item's rows
-  int r0;         // row offset of the item's row 0 from qbase's row 0
-  int R;          // rows
-  int ctx;        // causal bound of the rows (see above)
-  int Lk;         // one past the last key
-  int klo;        // first key (a tile boundary unless a sliding window sets it)
-  int grouped;    // 1: part of a prefix group, so its rows always go to partials
-};
-static_assert(sizeof(ItemDesc) == 32, "item size");
-
-// Items of a batch of B sequences: the sequences and at most B row blocks
-// (a group of m sequences is stacked only when it needs fewer than m blocks).
-__host__ __device__ inline int max_items(int B) { return 2 * B; }
-
-// Key tiles of an item: [klo / tile_keys, ceil(Lk / tile_keys)).
-__host__ __device__ inline int item_first_tile(const ItemDesc& d, int tile_keys) {
-  return d.klo / tile_keys;
-}
-__host__ __device__ inline int item_tiles(const ItemDesc& d, int tile_keys) {
-  const int n = (d.Lk + tile_keys - 1) / tile_keys - d.klo / tile_keys;
-  return n > 0 ? n : 0;
-}
-
 // Byte offsets of the workspace regions (all 256-aligned).
 struct WorkspaceLayout {
   size_t q_off;        // int32 [B+1]   first token row of each sequence
   size_t seq_T;        // int32 [B]     validated block length (0 if skipped)
   size_t seq_ctx;      // int32 [B]
   size_t seq_class;    // int32 [B]     kClassTensor / kClassSimt / -1
-  size_t seq_grp;      // int2  [B]     prefix group: first row-block item (-1: none),
-                       //               offset of the sequence's row 0 in the group's stacked rows
-  size_t items;        // ItemDesc [2B] tensor-core work items
-  size_t stp0;         // int32 [2B+1]  exclusive prefix of tiles per item (tensor-core class)
-  size_t stp1;         // int32 [B+1]   exclusive prefix of tiles per sequence (CUDA-core class)
-  size_t nseg;         // int32 [2B*Hkv] CTAs (segments) that cover the unit
-  size_t cfirst;       // int32 [2B*Hkv] first CTA of the unit
-  size_t part_base;    // int32 [2B*Hkv] first partial row of the unit, -1: rows go to the output
-  size_t wcost0;       // int64 [2B+1]  exclusive prefix of item costs (tensor-core class)
-  size_t wcost1;       // int64 [B+1]   exclusive prefix of sequence costs (CUDA-core class)
+  size_t stp;          // int32 [2][B+1] per-class exclusive prefix of tiles per sequence
+  size_t nseg;         // int32 [B*Hkv] CTAs (segments) that cover the unit
+  size_t cfirst;       // int32 [B*Hkv] first CTA of the unit
+  size_t part_base;    // int32 [B*Hkv] first partial row of the unit
+  size_t wcost;        // int64 [2][B+1] per-class exclusive prefix of sequence costs
   size_t cta_start;    // int32 [2][kMaxCtas+1] first tile of each CTA, per class
   size_t o_part;       // fp32  [rows_bound, D]
   size_t lse_part;     // fp32  [rows_bound]
@@ -137,21 +95,16 @@ __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_
 
 __host__ __device__ inline WorkspaceLayout make_layout(int B, int Hkv, int D, long long rows_bound) {
   WorkspaceLayout L;
-  const size_t NI = (size_t)max_items(B);
   size_t o = align256(sizeof(PlanHeader));
   L.q_off = o;      o = align256(o + sizeof(int) * (size_t)(B + 1));
   L.seq_T = o;      o = align256(o + sizeof(int) * (size_t)B);
   L.seq_ctx = o;    o = align256(o + sizeof(int) * (size_t)B);
   L.seq_class = o;  o = align256(o + sizeof(int) * (size_t)B);
-  L.seq_grp = o;    o = align256(o + sizeof(int2) * (size_t)B);
-  L.items = o;      o = align256(o + sizeof(ItemDesc) * NI);
-  L.stp0 = o;       o = align256(o + sizeof(int) * (NI + 1));
-  L.stp1 = o;       o = align256(o + sizeof(int) * (size_t)(B + 1));
-  L.nseg = o;       o = align256(o + sizeof(int) * NI * Hkv);
-  L.cfirst = o;     o = align256(o + sizeof(int) * NI * Hkv);
-  L.part_base = o;  o = align256(o + sizeof(int) * NI * Hkv);
-  L.wcost0 = o;     o = align256(o + sizeof(long long) * (NI + 1));
-  L.wcost1 = o;     o = align256(o + sizeof(long long) * (size_t)(B + 1));
+  L.stp = o;        o = align256(o + sizeof(int) * (size_t)kNumClasses * (B + 1));
+  L.nseg = o;       o = align256(o + sizeof(int) * (size_t)B * Hkv);
+  L.cfirst = o;     o = align256(o + sizeof(int) * (size_t)B * Hkv);
+  L.part_base = o;  o = align256(o + sizeof(int) * (size_t)B * Hkv);
+  L.wcost = o;      o = align256(o + sizeof(long long) * (size_t)kNumClasses * (B + 1));
   L.cta_start = o;  o = align256(o + sizeof(int) * (size_t)kNumClasses * (kMaxCtas + 1));
   L.o_part = o;     o = align256(o + sizeof(float) * (size_t)rows_bound * D);
   L.lse_part = o;   o = align256(o + sizeof(float) * (size_t)rows_bound);

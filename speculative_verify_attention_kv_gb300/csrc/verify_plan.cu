@@ -27,19 +27,12 @@ constexpr int kPlanSmallSeqs = 128;
 // Batches up to this many sequences keep the planner's per-sequence arrays in
 // shared memory as well (the later passes read them back many times; from
 // global memory each read would cost an L2 round trip).
-constexpr int kPlanSmemSeqs = kPrefixGroupMaxSeqs;
+constexpr int kPlanSmemSeqs = 1024;
 
-// The planner's shared-memory arrays for batches of up to kPlanSmemSeqs
-// sequences: per sequence T, ctx, class and the prefix sums per class (the
-// tensor-core ones per item); with prefix groups also the Q row offsets, the
-// links and stacked prefixes, and the rows and tiles of every item.
 struct PlanSmem {
-  int T[kPlanSmemSeqs], ctx[kPlanSmemSeqs], cls[kPlanSmemSeqs], qo[kPlanSmemSeqs];
-  int sl[kPlanSmemSeqs];                       // keys shared with the previous sequence (0: none)
-  int pg[kPlanSmemSeqs];                       // stacked prefix keys of the sequence's group (0: none)
-  int iR[2 * kPlanSmemSeqs], itiles[2 * kPlanSmemSeqs];   // rows and tiles of each item
-  int stp0[2 * kPlanSmemSeqs + 1], stp1[kPlanSmemSeqs + 1];
-  long long wcost0[2 * kPlanSmemSeqs + 1], wcost1[kPlanSmemSeqs + 1];
+  int T[kPlanSmemSeqs], ctx[kPlanSmemSeqs], cls[kPlanSmemSeqs];
+  int stp[kNumClasses][kPlanSmemSeqs + 1];
+  long long wcost[kNumClasses][kPlanSmemSeqs + 1];
 };
 
 // Inclusive max-scans of two values over the CTA (any multiple of 32 threads).
@@ -71,9 +64,8 @@ __device__ inline int2 block_inclusive_max2(int2 v, int2* s_warp) {
   return res;
 }
 
-// Per-sequence sums of pass 1: Q/O rows laid out, key tiles and estimated
-// cost per class; the item pass of a plan with prefix groups sums the
-// tensor-core class's tiles and cost over items (in w0 / t0).
+// The per-sequence quantities pass 1 sums: Q/O rows laid out, key tiles and
+// estimated cost per class.
 struct PlanSums {
   long long q, w0, w1;
   int t0, t1;
@@ -144,20 +136,11 @@ __device__ inline V block_exclusive_scan(V v, V* s_warp, V* total) {
   return res;
 }
 
-// shared_lens (may be null): shared_lens[b] keys at the start of sequence b's
-// context sit in the same pages as sequence b - 1's. With it (and no window),
-// a run of consecutive tensor-core sequences linked this way is a prefix
-// group: its sequences' rows, stacked in order, are cut into row blocks of
-// kMaxRows, and each block reads the group's common prefix (the smallest link,
-// cut to the sequences' contexts and down to a whole tile) once for all of its
-// rows; each sequence then reads only its keys after the prefix. A group is
-// stacked only when it needs fewer blocks than it has sequences.
 __global__ void __launch_bounds__(kPlanThreadsLarge)
 plan_kernel(const int32_t* __restrict__ context_lens, const int32_t* __restrict__ block_lens,
-            const int32_t* __restrict__ shared_lens, int num_seqs, int num_kv_heads, int group,
-            int max_pages, int max_block_len, int tile_tc, int tile_simt, int ncta_tc,
-            int ncta_simt, int path, int rows_bound, int num_q_tokens, int window,
-            unsigned char* ws, int* device_status) {
+            int num_seqs, int num_kv_heads, int group, int max_pages, int max_block_len,
+            int tile_tc, int tile_simt, int ncta_tc, int ncta_simt, int path, int rows_bound,
+            int num_q_tokens, int window, unsigned char* ws, int* device_status) {
   __shared__ int s_warp[32];
   __shared__ int2 s_warp2[32];
   __shared__ PlanSums s_sums[32];
@@ -165,29 +148,22 @@ plan_kernel(const int32_t* __restrict__ context_lens, const int32_t* __restrict_
   extern __shared__ __align__(16) unsigned char s_dyn[];
   allow_dependent_launch();        // the attention kernel may get its SMs now
   const bool small = num_seqs <= kPlanSmemSeqs;     // launched with sizeof(PlanSmem) then
-  // prefix groups are possible: the plan then has an item table
-  const bool grp = shared_lens != nullptr && small && window == 0;
   PlanSmem* ps = reinterpret_cast<PlanSmem*>(s_dyn);
   const WorkspaceLayout L = make_layout(num_seqs, num_kv_heads, 0, rows_bound);
   int* q_off = reinterpret_cast<int*>(ws + L.q_off);
   int* seq_T = reinterpret_cast<int*>(ws + L.seq_T);
   int* seq_ctx = reinterpret_cast<int*>(ws + L.seq_ctx);
   int* seq_class = reinterpret_cast<int*>(ws + L.seq_class);
-  int2* seq_grp = reinterpret_cast<int2*>(ws + L.seq_grp);
-  ItemDesc* items = reinterpret_cast<ItemDesc*>(ws + L.items);
-  int* stp0 = reinterpret_cast<int*>(ws + L.stp0);
-  int* stp1 = reinterpret_cast<int*>(ws + L.stp1);
+  int* stp = reinterpret_cast<int*>(ws + L.stp);
   int* nseg = reinterpret_cast<int*>(ws + L.nseg);
   int* cfirst = reinterpret_cast<int*>(ws + L.cfirst);
   int* part_base = reinterpret_cast<int*>(ws + L.part_base);
-  long long* wcost0 = reinterpret_cast<long long*>(ws + L.wcost0);
-  long long* wcost1 = reinterpret_cast<long long*>(ws + L.wcost1);
+  long long* wcost = reinterpret_cast<long long*>(ws + L.wcost);
   int* cta_start = reinterpret_cast<int*>(ws + L.cta_start);
   const int tile[kNumClasses] = {tile_tc, tile_simt};
   const int ncta[kNumClasses] = {ncta_tc, ncta_simt};
 
-  // pass 1: per sequence — validate, classify, prefix sums of rows and of
-  // tiles and cost per class; sequence b's tensor-core item is item b.
+  // pass 1: per sequence — validate, classify, prefix sums of rows and tiles.
   // The Q / O rows of sequence b start at the sum of the caller's block_lens
   // before it (negative lengths count as 0), whether or not b itself is valid:
   // a rejected sequence is idle, and the others keep their rows.
@@ -217,13 +193,11 @@ plan_kernel(const int32_t* __restrict__ context_lens, const int32_t* __restrict_
       seq_T[b] = T;
       seq_ctx[b] = ctx;
       seq_class[b] = cls;
-      if (shared_lens != nullptr) seq_grp[b] = make_int2(-1, 0);   // read by the combine then
       if (small) {
         ps->T[b] = T;
         ps->ctx[b] = ctx;
         ps->cls[b] = cls;
       }
-      if (grp) ps->pg[b] = 0;
     }
     // estimated cost of the sequence's units in its class (see tile_cost)
     long long cost = 0;
@@ -236,32 +210,16 @@ plan_kernel(const int32_t* __restrict__ context_lens, const int32_t* __restrict_
     const PlanSums ex = block_exclusive_scan_sums(mine, s_sums, &tot);
     if (b < num_seqs) {
       // offsets past the caller's rows only occur when the plan is dropped below
-      const int qo = (int)min(run_q + ex.q, (long long)num_q_tokens);
-      q_off[b] = qo;
-      stp0[b] = run_t0 + ex.t0;
-      stp1[b] = run_t1 + ex.t1;
-      wcost0[b] = run_w[0] + ex.w0;
-      wcost1[b] = run_w[1] + ex.w1;
-      if (grp) {                   // the sequence's item (the item walk reads it)
-        ItemDesc d;
-        d.b = b;
-        d.qbase = qo;
-        d.r0 = 0;
-        d.R = T * group;
-        d.ctx = ctx;
-        d.Lk = cls == kClassTensor ? ctx + T : 0;           // no tensor-core tiles otherwise
-        d.klo = cls == kClassTensor ? unit_first_key(ctx, window) : 0;
-        d.grouped = 0;
-        items[b] = d;
-        ps->qo[b] = qo;
-        ps->iR[b] = d.R;
-        ps->itiles[b] = cls == kClassTensor ? tiles : 0;
-      }
+      q_off[b] = (int)min(run_q + ex.q, (long long)num_q_tokens);
+      stp[b] = run_t0 + ex.t0;
+      stp[(num_seqs + 1) + b] = run_t1 + ex.t1;
+      wcost[b] = run_w[0] + ex.w0;
+      wcost[(num_seqs + 1) + b] = run_w[1] + ex.w1;
       if (small) {
-        ps->stp0[b] = run_t0 + ex.t0;
-        ps->stp1[b] = run_t1 + ex.t1;
-        ps->wcost0[b] = run_w[0] + ex.w0;
-        ps->wcost1[b] = run_w[1] + ex.w1;
+        ps->stp[0][b] = run_t0 + ex.t0;
+        ps->stp[1][b] = run_t1 + ex.t1;
+        ps->wcost[0][b] = run_w[0] + ex.w0;
+        ps->wcost[1][b] = run_w[1] + ex.w1;
       }
     }
     run_q += tot.q;
@@ -272,22 +230,19 @@ plan_kernel(const int32_t* __restrict__ context_lens, const int32_t* __restrict_
   }
   if (threadIdx.x == 0) {
     q_off[num_seqs] = (int)min(run_q, (long long)num_q_tokens);
-    stp0[num_seqs] = run_t0;
-    stp1[num_seqs] = run_t1;
-    wcost0[num_seqs] = run_w[0];
-    wcost1[num_seqs] = run_w[1];
+    stp[num_seqs] = run_t0;
+    stp[(num_seqs + 1) + num_seqs] = run_t1;
+    for (int c = 0; c < kNumClasses; ++c) wcost[c * (num_seqs + 1) + num_seqs] = run_w[c];
     if (small) {
-      ps->stp0[num_seqs] = run_t0;
-      ps->stp1[num_seqs] = run_t1;
-      ps->wcost0[num_seqs] = run_w[0];
-      ps->wcost1[num_seqs] = run_w[1];
+      ps->stp[0][num_seqs] = run_t0;
+      ps->stp[1][num_seqs] = run_t1;
+      for (int c = 0; c < kNumClasses; ++c) ps->wcost[c][num_seqs] = run_w[c];
     }
   }
   __syncthreads();
   // where the later passes read the per-sequence arrays
   const int* rT = small ? ps->T : seq_T;
   const int* rctx = small ? ps->ctx : seq_ctx;
-  const int* rcls = small ? ps->cls : seq_class;
   // block lengths that sum past the q / out rows the caller passed: do nothing
   const bool rows_ok = run_q <= num_q_tokens;
   if (!rows_ok) {
@@ -299,120 +254,6 @@ plan_kernel(const int32_t* __restrict__ context_lens, const int32_t* __restrict_
     }
     __syncthreads();
   }
-
-  // prefix groups (tensor-core class; items num_seqs.. are their row blocks)
-  int num_blocks = 0;
-  if (grp && rows_ok) {
-    // link of b to b - 1: the shared keys, cut to both contexts; 0 below a tile
-    for (int b = threadIdx.x; b < num_seqs; b += blockDim.x) {
-      int sl = 0;
-      if (b > 0 && ps->cls[b] == kClassTensor && ps->cls[b - 1] == kClassTensor) {
-        sl = min(shared_lens[b], min(ps->ctx[b], ps->ctx[b - 1]));
-        if (sl < tile_tc) sl = 0;
-      }
-      ps->sl[b] = sl;
-    }
-    __syncthreads();
-    // the first sequence of each group walks its group
-    for (int base = 0; base < num_seqs; base += (int)blockDim.x) {
-      const int b = base + threadIdx.x;
-      int nblk = 0, m = 0, pg = 0, rows = 0;
-      if (b < num_seqs && ps->cls[b] == kClassTensor && ps->sl[b] == 0 && b + 1 < num_seqs &&
-          ps->sl[b + 1] > 0) {
-        pg = ps->ctx[b];
-        rows = ps->T[b] * group;
-        int e = b + 1;
-        for (; e < num_seqs && ps->sl[e] > 0; ++e) {
-          pg = min(pg, ps->sl[e]);
-          rows += ps->T[e] * group;
-        }
-        m = e - b;
-        pg = pg / tile_tc * tile_tc;
-        nblk = (rows + kMaxRows - 1) / kMaxRows;
-        if (pg < tile_tc || nblk >= m) nblk = 0;     // stacking would not save a pass
-      }
-      int tot;
-      const int ex = block_exclusive_scan(nblk, s_warp, &tot);
-      if (nblk > 0) {
-        const int first_item = num_seqs + num_blocks + ex;
-        int so = 0;
-        for (int e = b; e < b + m; ++e) {
-          // the member reads only its keys past the prefix
-          seq_grp[e] = make_int2(first_item, so);
-          ps->pg[e] = pg;
-          items[e].klo = pg;
-          items[e].grouped = 1;
-          ps->itiles[e] = (ps->ctx[e] + ps->T[e] + tile_tc - 1) / tile_tc - pg / tile_tc;
-          so += ps->T[e] * group;
-        }
-        for (int k = 0; k < nblk; ++k) {
-          ItemDesc d;
-          d.b = b;
-          d.qbase = ps->qo[b];
-          d.r0 = k * kMaxRows;
-          d.R = min(kMaxRows, rows - k * kMaxRows);
-          d.ctx = pg;
-          d.Lk = pg;
-          d.klo = 0;
-          d.grouped = 1;
-          items[first_item + k] = d;
-          ps->iR[first_item + k] = d.R;
-          ps->itiles[first_item + k] = pg / tile_tc;
-        }
-      }
-      num_blocks += tot;
-    }
-    __syncthreads();
-    if (num_blocks > 0) {
-      // the tensor-core class's prefix sums again, over all items
-      run_t0 = 0;
-      run_w[0] = 0;
-      const int ni = num_seqs + num_blocks;
-      for (int base = 0; base < ni; base += (int)blockDim.x) {
-        const int i = base + threadIdx.x;
-        const int tiles = i < ni ? ps->itiles[i] : 0;
-        long long cost = 0;
-        if (tiles > 0)
-          cost = (long long)num_kv_heads *
-                 ((long long)tiles * (tile_cost(0) + row_cost(0) * ps->iR[i]) + segment_cost(0));
-        const PlanSums mine{0, cost, 0, tiles * num_kv_heads, 0};
-        PlanSums tot;
-        const PlanSums ex = block_exclusive_scan_sums(mine, s_sums, &tot);
-        if (i < ni) {
-          stp0[i] = run_t0 + ex.t0;
-          wcost0[i] = run_w[0] + ex.w0;
-          ps->stp0[i] = run_t0 + ex.t0;
-          ps->wcost0[i] = run_w[0] + ex.w0;
-        }
-        run_t0 += tot.t0;
-        run_w[0] += tot.w0;
-      }
-      if (threadIdx.x == 0) {
-        stp0[ni] = run_t0;
-        wcost0[ni] = run_w[0];
-        ps->stp0[ni] = run_t0;
-        ps->wcost0[ni] = run_w[0];
-      }
-      __syncthreads();
-    }
-  }
-  const int num_items = num_seqs + num_blocks;
-  // the attention kernel's item walk searches max_items(num_seqs) entries of
-  // stp0: the ones past the items must exceed every tile index
-  if (grp)
-    for (int i = num_items + 1 + threadIdx.x; i <= max_items(num_seqs); i += blockDim.x)
-      stp0[i] = INT_MAX;
-
-  // rows and tensor-core tiles of item i
-  auto item_shape = [&](int i, int& R, int& tiles) {
-    if (grp) {
-      R = ps->iR[i];
-      tiles = ps->itiles[i];
-    } else {                       // one item per sequence
-      R = rT[i] * group;
-      tiles = rcls[i] == kClassTensor ? unit_tiles(rctx[i], rT[i], window, tile_tc) : 0;
-    }
-  };
   const int total[kNumClasses] = {run_t0, run_t1};
   // a class's kernel uses at most one CTA per tile, so that every CTA it uses
   // owns >= 1 tile and the CTAs covering a unit are consecutive, all non-empty
@@ -420,7 +261,7 @@ plan_kernel(const int32_t* __restrict__ context_lens, const int32_t* __restrict_
   for (int c = 0; c < kNumClasses; ++c) ncta_eff[c] = min(min(ncta[c], total[c]), kMaxCtas);
 
   // CTA c of a class starts where the class's cumulative cost reaches
-  // c / n of its total: find the item (sequence), then the unit (KV head), then the
+  // c / n of its total: find the sequence, then the unit (KV head), then the
   // tile (the first segment_cost of a unit maps to its first tile). Then the
   // starts are made strictly increasing (every CTA owns >= 1 tile) and the
   // last ones are pulled back so that CTA n - 1 still fits before `total`.
@@ -435,33 +276,23 @@ plan_kernel(const int32_t* __restrict__ context_lens, const int32_t* __restrict_
 #pragma unroll
       for (int c = 0; c < kNumClasses; ++c) {
         const int n = ncta_eff[c];
-        if (k <= n && n > 0) {
+        const long long* wc = small ? ps->wcost[c] : wcost + c * (num_seqs + 1);
+        const int* sp = small ? ps->stp[c] : stp + c * (num_seqs + 1);
+        if (k <= n && n > 0 && rows_ok) {
           if (k == n) {
             start[c] = total[c];
           } else if (k > 0) {
             const long long target = run_w[c] * k / n;      // < 2^63 for any realistic batch
-            int b, tiles, R, sp;
-            long long off;
-            if (c == 0) {
-              const long long* wc = small ? ps->wcost0 : wcost0;
-              b = upper_index(wc, num_items - 1, target);
-              off = target - wc[b];
-              item_shape(b, R, tiles);
-              sp = small ? ps->stp0[b] : stp0[b];
-            } else {
-              const long long* wc = small ? ps->wcost1 : wcost1;
-              b = upper_index(wc, num_seqs - 1, target);
-              off = target - wc[b];
-              tiles = unit_tiles(rctx[b], rT[b], window, tile[1]);
-              R = rT[b] * group;
-              sp = small ? ps->stp1[b] : stp1[b];
-            }
-            const long long w = tile_cost(c) + row_cost(c) * R;
+            const int b = upper_index(wc, num_seqs - 1, target);
+            const long long off = target - wc[b];
+            const int T = rT[b];
+            const int tiles = unit_tiles(rctx[b], T, window, tile[c]);
+            const long long w = tile_cost(c) + row_cost(c) * T * group;
             const long long uc = (long long)tiles * w + segment_cost(c);
             const int h = (int)min(off / uc, (long long)num_kv_heads - 1);
             const long long rem = off - h * uc;
             const int t = rem < segment_cost(c) ? 0 : (int)min((rem - segment_cost(c)) / w, (long long)tiles - 1);
-            start[c] = sp + h * tiles + t;
+            start[c] = sp[b] + h * tiles + t;
           }
         }
       }
@@ -484,42 +315,34 @@ plan_kernel(const int32_t* __restrict__ context_lens, const int32_t* __restrict_
     for (int k = threadIdx.x; k <= ncta_eff[c]; k += blockDim.x)
       cta_start[c * (kMaxCtas + 1) + k] = s_start[c][k];
 
-  // pass 2: per unit (item or sequence i, KV head h) — segments and partial
-  // rows. Units i * Hkv + h with i < num_seqs are sequence i's (the CUDA-core
-  // kernel's when the sequence is in its class).
-  const int num_units = num_items * num_kv_heads;
+  // pass 2: per unit (b, h) — segments and partial rows
+  const int num_units = num_seqs * num_kv_heads;
   int run_rows = 0;
   for (int base = 0; base < num_units; base += (int)blockDim.x) {
     const int u = base + threadIdx.x;
-    int rows = 0, ns = 0, cf = 0;
+    int rows = 0;
     if (u < num_units) {
-      const int i = u / num_kv_heads, h = u % num_kv_heads;
-      const bool simt = i < num_seqs && rcls[i] == kClassSimt;
-      int tiles, R, grouped, tp;
-      if (simt) {
-        tiles = unit_tiles(rctx[i], rT[i], window, tile[1]);
-        R = rT[i] * group;
-        grouped = 0;
-        tp = (small ? ps->stp1[i] : stp1[i]) + h * tiles;
-      } else {
-        item_shape(i, R, tiles);
-        grouped = grp && (i >= num_seqs || ps->pg[i] > 0);
-        tp = (small ? ps->stp0[i] : stp0[i]) + h * tiles;
-      }
-      const int nce = simt ? ncta_eff[1] : ncta_eff[0];
-      if (tiles > 0 && nce > 0) {
-        const int* cs = s_start[simt ? 1 : 0];
+      const int b = u / num_kv_heads, h = u % num_kv_heads;
+      const int cls = small ? ps->cls[b] : seq_class[b];
+      int ns = 0, cf = 0;
+      if (cls >= 0) {
+        const int T = rT[b], ctx = rctx[b];
+        const int tk = cls == 0 ? tile[0] : tile[1];        // selects, not a local-memory index
+        const int nce = cls == 0 ? ncta_eff[0] : ncta_eff[1];
+        const int tiles = unit_tiles(ctx, T, window, tk);
+        const int tp = (small ? ps->stp[cls][b] : stp[cls * (num_seqs + 1) + b]) + h * tiles;
+        const int* cs = s_start[cls == 0 ? 0 : 1];
         cf = upper_index(cs, nce - 1, tp);
         const int cl = upper_index(cs, nce - 1, tp + tiles - 1);
         ns = cl - cf + 1;
-        if (ns > 1 || grouped) rows = ns * R;
+        if (ns > 1) rows = ns * T * group;
       }
       nseg[u] = ns;
       cfirst[u] = cf;
     }
     int tot;
     const int pb = block_exclusive_scan(rows, s_warp, &tot);
-    if (u < num_units) part_base[u] = rows > 0 ? run_rows + pb : -1;
+    if (u < num_units) part_base[u] = run_rows + pb;
     run_rows += tot;
   }
   if (threadIdx.x == 0) {
@@ -536,20 +359,15 @@ plan_kernel(const int32_t* __restrict__ context_lens, const int32_t* __restrict_
     hd->total_part_rows = run_rows;
     hd->rows_bound = rows_bound;
     hd->window = window;
-    hd->num_items = num_items;
   }
 }
 
-// WPR warps per (token row, query head) whose result is in partials: rows of a
-// unit split over several CTAs, and every row of a prefix group (its row
-// block's partials, then its own unit's). Warp `sub` of a row
+// WPR warps per (token row, query head) of a split unit; warp `sub` of a row
 // accumulates the partials j = sub, sub + WPR, ... (four or eight partial rows
 // in flight), and the WPR sums meet in shared memory. Every warp of a row reads all
 // lse_j in one pass (running max and rescaled sum per lane, then merged across
-// the warp), so the weights exp(lse_j - lse) agree across the row's warps->
-// kGroups: the plan may hold prefix groups (else the second source is never
-// looked up, and the kernel keeps the registers of the one-source loop).
-template <int D, int WPR, bool kGroups>
+// the warp), so the weights exp(lse_j - lse) agree across the row's warps.
+template <int D, int WPR>
 __global__ void __launch_bounds__(256, 2)
 lse_combine_kernel(int num_q_tokens, int num_q_heads, int num_seqs, int num_kv_heads, int group,
                    int rows_bound, const unsigned char* __restrict__ ws,
@@ -565,46 +383,27 @@ lse_combine_kernel(int num_q_tokens, int num_q_heads, int num_seqs, int num_kv_h
   const WorkspaceLayout L = make_layout(num_seqs, num_kv_heads, D, rows_bound);
   const int* q_off = reinterpret_cast<const int*>(ws + L.q_off);
   const int* seq_T = reinterpret_cast<const int*>(ws + L.seq_T);
-  const int2* seq_grp = reinterpret_cast<const int2*>(ws + L.seq_grp);
-  const ItemDesc* items = reinterpret_cast<const ItemDesc*>(ws + L.items);
   const int* nseg = reinterpret_cast<const int*>(ws + L.nseg);
   const int* part_base = reinterpret_cast<const int*>(ws + L.part_base);
   const float* o_part = reinterpret_cast<const float*>(ws + L.o_part);
   const float* lse_part = reinterpret_cast<const float*>(ws + L.lse_part);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, sub = warp % WPR;
   const long long row = (long long)blockIdx.x * kRowsPerBlock + warp / WPR;
-  // the warp's row, when its result is in partials: n1 of its own unit's
-  // (rows R1 apart from row r1 on), then n2 of its row block's (R2 apart from r2)
+  // the warp's row, when it belongs to a unit with two or more partials
   bool active = row < (long long)num_q_tokens * num_q_heads;
-  int i = 0, hq = 0, n1 = 0, n = 0, R1 = 0, r1 = 0, R2 = 0, r2 = 0;
-  long long base1 = 0, base2 = 0;
+  int i = 0, hq = 0, n = 0, R = 0, r = 0;
+  long long base = 0;
   if (active) {
     i = (int)(row / num_q_heads);
     hq = (int)(row % num_q_heads);
     const int b = upper_index(q_off, num_seqs - 1, i);
     const int h = hq / group, g = hq % group;
     const int u = b * num_kv_heads + h;
-    const int t = i - q_off[b];
-    const int T = seq_T[b];
-    n1 = nseg[u];
-    base1 = part_base[u];
-    active = t < T;
-    if (active) {
-      R1 = T * group;
-      r1 = t * group + g;
-      n = n1 > 1 ? n1 : 0;
-      const int2 gr = kGroups ? seq_grp[b] : make_int2(-1, 0);
-      if (kGroups && gr.x >= 0) {       // prefix group: its row block, and its own unit always
-        const int js = gr.y + r1;
-        const int it = gr.x + js / kMaxRows;
-        const int u2 = it * num_kv_heads + h;
-        R2 = items[it].R;
-        r2 = js % kMaxRows;
-        base2 = part_base[u2];
-        n = n1 + nseg[u2];
-      }
-      active = n > 0;
-    }
+    n = nseg[u];
+    active = n > 1 && i - q_off[b] < seq_T[b];
+    R = seq_T[b] * group;
+    r = (i - q_off[b]) * group + g;
+    base = part_base[u];
   }
   float acc[EPL];
 #pragma unroll
@@ -614,8 +413,7 @@ lse_combine_kernel(int num_q_tokens, int num_q_heads, int num_seqs, int num_kv_h
     // lse = m + ln(wsum) over all partials, one pass
     float sl = 0.f;
     for (int j = lane; j < n; j += 32) {
-      const float lj = lse_part[(!kGroups || j < n1) ? base1 + (long long)j * R1 + r1
-                                                      : base2 + (long long)(j - n1) * R2 + r2];
+      const float lj = lse_part[base + (long long)j * R + r];
       if (lj > m) {
         sl = sl * __expf(m - lj) + 1.f;     // m = -inf: sl is 0 and stays finite
         m = lj;
@@ -634,8 +432,7 @@ lse_combine_kernel(int num_q_tokens, int num_q_heads, int num_seqs, int num_kv_h
         const int j = j0 + k * WPR;
         w[k] = 0.f;
         if (j < n) {
-          const long long pr = (!kGroups || j < n1) ? base1 + (long long)j * R1 + r1
-                                                    : base2 + (long long)(j - n1) * R2 + r2;
+          const long long pr = base + (long long)j * R + r;
           const float lj = lse_part[pr];
           w[k] = (lj == -INFINITY) ? 0.f : __expf(lj - m);
           const Vec* src = reinterpret_cast<const Vec*>(o_part + pr * D + lane * EPL);
@@ -677,26 +474,22 @@ lse_combine_kernel(int num_q_tokens, int num_q_heads, int num_seqs, int num_kv_h
   if (lane == 0) lse_out[(long long)i * num_q_heads + hq] = m + logf(wsum);
 }
 
-cudaError_t launch_plan(const int32_t* context_lens, const int32_t* block_lens,
-                        const int32_t* shared_lens, int num_seqs, int num_kv_heads, int group,
-                        int max_pages, int max_block_len, int tile_tc, int tile_simt, int ncta_tc,
-                        int ncta_simt, int path, int rows_bound, int num_q_tokens, int window,
-                        unsigned char* ws, int* device_status, cudaStream_t stream) {
+cudaError_t launch_plan(const int32_t* context_lens, const int32_t* block_lens, int num_seqs,
+                        int num_kv_heads, int group, int max_pages, int max_block_len, int tile_tc,
+                        int tile_simt, int ncta_tc, int ncta_simt, int path, int rows_bound,
+                        int num_q_tokens, int window, unsigned char* ws, int* device_status,
+                        cudaStream_t stream) {
   const size_t dyn = num_seqs <= kPlanSmemSeqs ? sizeof(PlanSmem) : 0;
   const int threads = num_seqs <= kPlanSmallSeqs ? kPlanThreadsSmall : kPlanThreadsLarge;
-  if (dyn > 0) {
-    const cudaError_t e = ensure_dynamic_smem<plan_kernel>((int)dyn);
-    if (e != cudaSuccess) return e;
-  }
-  plan_kernel<<<1, threads, dyn, stream>>>(context_lens, block_lens, shared_lens, num_seqs,
-                                              num_kv_heads, group, max_pages, max_block_len,
-                                              tile_tc, tile_simt, ncta_tc, ncta_simt, path,
-                                              rows_bound, num_q_tokens, window, ws, device_status);
+  plan_kernel<<<1, threads, dyn, stream>>>(context_lens, block_lens, num_seqs, num_kv_heads,
+                                              group, max_pages, max_block_len, tile_tc, tile_simt,
+                                              ncta_tc, ncta_simt, path, rows_bound, num_q_tokens,
+                                              window, ws, device_status);
   return cudaGetLastError();
 }
 
 cudaError_t launch_combine(int num_q_tokens, int num_q_heads, int num_seqs, int num_kv_heads,
-                           int group, int head_dim, int rows_bound, int sms, bool prefix_groups,
+                           int group, int head_dim, int rows_bound, int sms,
                            const unsigned char* ws, __nv_bfloat16* out, float* lse,
                            cudaStream_t stream) {
   const long long rows = (long long)num_q_tokens * num_q_heads;
@@ -709,13 +502,9 @@ cudaError_t launch_combine(int num_q_tokens, int num_q_heads, int num_seqs, int 
   const int grid = (int)((rows + rows_per_block - 1) / rows_per_block);
   cudaError_t e = cudaErrorInvalidValue;
 #define SPLASH_COMBINE(DD, WW)                                                                  \
-  e = prefix_groups                                                                             \
-          ? launch_dependent(lse_combine_kernel<DD, WW, true>, dim3(grid), dim3(256), 0, stream, \
-                             num_q_tokens, num_q_heads, num_seqs, num_kv_heads, group,          \
-                             rows_bound, ws, out, lse)                                          \
-          : launch_dependent(lse_combine_kernel<DD, WW, false>, dim3(grid), dim3(256), 0,       \
-                             stream, num_q_tokens, num_q_heads, num_seqs, num_kv_heads, group,  \
-                             rows_bound, ws, out, lse)
+  e = launch_dependent(lse_combine_kernel<DD, WW>, dim3(grid), dim3(256), 0, stream,            \
+                       num_q_tokens, num_q_heads, num_seqs, num_kv_heads, group, rows_bound, ws, \
+                       out, lse)
 #define SPLASH_COMBINE_D(DD)          \
   switch (wpr) {                      \
     case 1: SPLASH_COMBINE(DD, 1); break; \

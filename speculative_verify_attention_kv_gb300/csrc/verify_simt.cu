@@ -53,7 +53,7 @@ verify_simt_kernel(AttnParams p, int rows_cap) {
   const int* q_off = reinterpret_cast<const int*>(p.ws + L.q_off);
   const int* seq_T = reinterpret_cast<const int*>(p.ws + L.seq_T);
   const int* seq_ctx = reinterpret_cast<const int*>(p.ws + L.seq_ctx);
-  const int* stp = reinterpret_cast<const int*>(p.ws + L.stp1);
+  const int* stp = reinterpret_cast<const int*>(p.ws + L.stp) + kClassSimt * (B + 1);
   const int* nseg = reinterpret_cast<const int*>(p.ws + L.nseg);
   const int* cfirst = reinterpret_cast<const int*>(p.ws + L.cfirst);
   const int* part_base = reinterpret_cast<const int*>(p.ws + L.part_base);

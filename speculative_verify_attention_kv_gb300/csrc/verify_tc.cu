@@ -51,6 +51,7 @@
 // dependent launch).
 #include <type_traits>
 
+#include "splash_groups.cuh"
 #include "tcgen05_ptx.cuh"
 
 namespace splash {
@@ -170,6 +171,17 @@ struct ItemSegIter {
     return true;
   }
 };
+
+// The plan's workspace layout: the plain one, or the one of a plan with
+// prefix groups (the same names for the regions the kernel reads).
+template <bool kItems>
+__device__ __forceinline__ typename std::conditional<kItems, GroupLayout, WorkspaceLayout>::type
+layout_for(int B, int Hkv, int D, long long rows_bound) {
+  if constexpr (kItems)
+    return make_group_layout(B, Hkv, D, rows_bound);
+  else
+    return make_layout(B, Hkv, D, rows_bound);
+}
 
 template <bool kItems>
 __device__ __forceinline__ typename std::conditional<kItems, ItemSegIter, SegIter>::type
@@ -416,12 +428,13 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(AttnParams p) {
     return;
   }
   const int B = p.num_seqs, Hkv = p.num_kv_heads, G = p.group;
-  const WorkspaceLayout L = make_layout(B, Hkv, D, hd->rows_bound);
+  const auto L = layout_for<kItems>(B, Hkv, D, hd->rows_bound);
   const int* q_off = reinterpret_cast<const int*>(p.ws + L.q_off);
   const int* seq_T = reinterpret_cast<const int*>(p.ws + L.seq_T);
   const int* seq_ctx = reinterpret_cast<const int*>(p.ws + L.seq_ctx);
-  const ItemDesc* items = reinterpret_cast<const ItemDesc*>(p.ws + L.items);
-  const int* stp = reinterpret_cast<const int*>(p.ws + L.stp0);
+  const ItemDesc* items = static_cast<const ItemDesc*>(nullptr);
+  if constexpr (kItems) items = reinterpret_cast<const ItemDesc*>(p.ws + L.items);
+  const int* stp = reinterpret_cast<const int*>(p.ws + L.stp) + kClassTensor * (B + 1);
   const int* nseg = reinterpret_cast<const int*>(p.ws + L.nseg);
   const int* cfirst = reinterpret_cast<const int*>(p.ws + L.cfirst);
   const int* part_base = reinterpret_cast<const int*>(p.ws + L.part_base);

@@ -282,7 +282,7 @@ verify_tt_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmap) {
   const int* q_off = reinterpret_cast<const int*>(p.ws + L.q_off);
   const int* seq_T = reinterpret_cast<const int*>(p.ws + L.seq_T);
   const int* seq_ctx = reinterpret_cast<const int*>(p.ws + L.seq_ctx);
-  const int* stp = reinterpret_cast<const int*>(p.ws + L.stp0);   // one item per sequence (no prefix groups)
+  const int* stp = reinterpret_cast<const int*>(p.ws + L.stp) + kClassTensor * (B + 1);
   const int* nseg = reinterpret_cast<const int*>(p.ws + L.nseg);
   const int* cfirst = reinterpret_cast<const int*>(p.ws + L.cfirst);
   const int* part_base = reinterpret_cast<const int*>(p.ws + L.part_base);

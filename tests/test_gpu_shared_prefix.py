@@ -73,7 +73,8 @@ def expected_plan(ctx, T, shared_lens, G, Hkv):
 
 
 def plan_header(ws):
-    """(total tensor-core tiles, items) from the plan header the planner wrote."""
+    """(total tensor-core tiles, items) from the plan header the prefix-group
+    planner wrote (it keeps the item count in the header's first spare word)."""
     h = ws[:64].cpu().numpy().view(np.int32)
     return int(h[0]), int(h[12])
 
@@ -186,8 +187,6 @@ def test_paths_without_groups_compute_the_same_result(path):
     torch.cuda.synchronize()
     assert int(r.status.item()) == 0
     assert_parity(out, lse, o_ref, l_ref, what=f"path {path}")
-    _, items = plan_header(r.ws)
-    assert items == len(c["ctx"])
 
 
 def test_zero_links_plan_like_the_plain_call():
