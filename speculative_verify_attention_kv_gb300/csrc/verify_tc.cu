@@ -49,6 +49,11 @@
 // cost) and the units' segment layout come from the split planner; barriers
 // and TMEM are set up before the kernel waits for the plan (programmatic
 // dependent launch).
+// With prefix groups (kItems) a unit is (work item, KV head) instead: a row
+// block of several sequences' stacked rows against their common prefix keys,
+// or one sequence's rows against its keys after the prefix. The item table
+// gives each segment its page-table row, first query token, row offset and
+// key range; the pipeline above is the same.
 #include <type_traits>
 
 #include "splash_groups.cuh"
