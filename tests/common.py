@@ -80,3 +80,44 @@ def quantise_row_exact(x):
         return [0] * len(xs), 0.0
     codes = [max(-127, min(127, round_half_even_exact(round_to_f32(v / s)))) for v in xs]
     return codes, float(s)
+
+
+# ---- the prefix-group rule of splash_verify_attention_shared ---------------
+GROUP_TILE, GROUP_MAX_ROWS = 64, 128
+
+
+def expected_group_plan(ctx, T, shared_lens, G, Hkv):
+    """(items, tensor-core tiles of all units) under the grouping rule the
+    header states: b links to b - 1 when both have a block and
+    min(shared_lens[b], ctx[b], ctx[b-1]) >= 64; a maximal linked run is a
+    group whose prefix is its smallest link (cut to every context) rounded down
+    to 64 keys; it is stacked when ceil(sum T*G / 128) < its size, as that many
+    row blocks over the prefix, each member then reading its keys after it."""
+    B = len(ctx)
+    link = [0] * B
+    for b in range(1, B):
+        if T[b] > 0 and T[b - 1] > 0:
+            s = min(shared_lens[b], ctx[b], ctx[b - 1])
+            link[b] = s if s >= GROUP_TILE else 0
+    pg_of = [0] * B
+    blocks = []                                   # prefix keys of each row block
+    b = 0
+    while b < B:
+        e = b + 1
+        while e < B and link[e] > 0:
+            e += 1
+        if T[b] > 0 and e - b > 1:
+            pg = min([ctx[b]] + link[b + 1:e]) // GROUP_TILE * GROUP_TILE
+            rows = sum(T[i] * G for i in range(b, e))
+            nblk = -(-rows // GROUP_MAX_ROWS)
+            if pg >= GROUP_TILE and nblk < e - b:
+                for i in range(b, e):
+                    pg_of[i] = pg
+                blocks += [pg] * nblk
+        b = e
+    tiles = 0
+    for i in range(B):
+        if T[i] > 0:
+            tiles += -(-(ctx[i] + T[i]) // GROUP_TILE) - pg_of[i] // GROUP_TILE
+    tiles += sum(pg // GROUP_TILE for pg in blocks)
+    return B + len(blocks), tiles * Hkv

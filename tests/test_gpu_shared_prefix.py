@@ -30,47 +30,8 @@ if not os.path.exists(_build.LIB):
 from speculative_verify_attention_kv_gb300 import splash_kv as sk  # noqa: E402
 from speculative_verify_attention_kv_gb300 import workloads as wl  # noqa: E402
 
-from common import oracle_pool, q_values  # noqa: E402
+from common import expected_group_plan as expected_plan, oracle_pool, q_values  # noqa: E402
 from gpu_common import Run, assert_parity  # noqa: E402
-
-TILE, MAX_ROWS = 64, 128
-
-
-def expected_plan(ctx, T, shared_lens, G, Hkv):
-    """(items, tensor-core tiles of all units) under the header's grouping
-    rule: b links to b - 1 when both have a block and min(shared_lens[b],
-    ctx[b], ctx[b-1]) >= 64; a maximal linked run is a group whose prefix is
-    its smallest link (cut to every context) rounded down to 64 keys; it is
-    stacked when ceil(sum T*G / 128) < its size."""
-    B = len(ctx)
-    link = [0] * B
-    for b in range(1, B):
-        if T[b] > 0 and T[b - 1] > 0:
-            s = min(shared_lens[b], ctx[b], ctx[b - 1])
-            link[b] = s if s >= TILE else 0
-    pg_of = [0] * B
-    blocks = []                                   # (prefix keys) per row block
-    b = 0
-    while b < B:
-        e = b + 1
-        while e < B and link[e] > 0:
-            e += 1
-        if T[b] > 0 and e - b > 1:
-            pg = min([ctx[b]] + link[b + 1:e]) // TILE * TILE
-            rows = sum(T[i] * G for i in range(b, e))
-            nblk = -(-rows // MAX_ROWS)
-            if pg >= TILE and nblk < e - b:
-                for i in range(b, e):
-                    pg_of[i] = pg
-                blocks += [pg] * nblk
-        b = e
-    tiles = 0
-    for i in range(B):
-        if T[i] > 0:
-            tiles += -(-(ctx[i] + T[i]) // TILE) - pg_of[i] // TILE
-    tiles += sum(pg // TILE for pg in blocks)
-    return B + len(blocks), tiles * Hkv
-
 
 def plan_header(ws):
     """(total tensor-core tiles, items) from the plan header the prefix-group
